@@ -1,0 +1,264 @@
+"""Thin ctypes binding of libivfpq_gb300.so (include/ivfpq.h).
+
+Argument marshalling only: every function here checks shapes and dtypes of
+torch CUDA tensors, passes their device pointers and the current CUDA stream
+to the C entry point of the same name, and raises :class:`IVFPQError` on a
+non-zero status. No computation happens in Python and there is no CPU
+fallback: if the library has not been built, :class:`LibraryMissing` is
+raised.
+"""
+
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libivfpq_gb300.so")
+
+IVFPQ_OK = 0
+IVFPQ_ERR_INVALID_ARG = -1
+IVFPQ_ERR_UNSUPPORTED = -2
+IVFPQ_ERR_OOM = -3
+IVFPQ_ERR_CUDA = -4
+IVFPQ_ERR_DEVICE_CHECK = -5
+IVFPQ_ERR_TIMEOUT = -6
+
+LUT_FP32, LUT_FP16, LUT_FP8 = 0, 1, 2
+LUT_TYPES = {"fp32": LUT_FP32, "fp16": LUT_FP16, "fp8": LUT_FP8}
+MAX_K = 2048
+
+# name -> (restype, argtypes); mirrors include/ivfpq.h
+_VP, _I, _I64 = C.c_void_p, C.c_int, C.c_int64
+SIGNATURES = {
+    "ivfpq_index_create": (_I, [_I, _I, _I, _I, _VP, _VP, C.POINTER(_VP)]),
+    "ivfpq_index_destroy": (_I, [_VP]),
+    "ivfpq_set_lut_type": (_I, [_VP, _I]),
+    "ivfpq_add": (_I, [_VP, _VP, _VP, _VP, _I64, _VP]),
+    "ivfpq_ntotal": (_I64, [_VP]),
+    "ivfpq_search": (_I, [_VP, _VP, _I64, _I, _I, _VP, _VP, _VP]),
+    "ivfpq_search_probes": (_I, [_VP, _VP, _I64, _I, _VP, _VP, _VP]),
+    "ivfpq_search_preassigned": (_I, [_VP, _VP, _I64, _I, _VP, _I, _VP, _VP, _VP]),
+    "ivfpq_set_profiling": (_I, [_VP, _I]),
+    "ivfpq_stage_times": (_I, [_VP, C.POINTER(C.c_float)]),
+    "flat_knn": (_I, [_VP, _I64, _I, _VP, _I64, _I, _VP, _VP, _VP]),
+    "kselect": (_I, [_VP, _I64, _I64, _I, _VP, _VP, _VP]),
+    "ivfpq_last_error": (C.c_char_p, []),
+    "ivfpq_status_string": (C.c_char_p, [_I]),
+}
+
+
+class LibraryMissing(RuntimeError):
+    pass
+
+
+class IVFPQError(RuntimeError):
+    def __init__(self, fn, status, msg):
+        super().__init__(f"{fn} failed with status {status}: {msg}")
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def lib():
+    """The loaded library (raises LibraryMissing if it was never built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise LibraryMissing(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = C.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                f = getattr(L, name)
+                f.restype = res
+                f.argtypes = args
+            _lib = L
+    return _lib
+
+
+def _check(fn, status):
+    if status != IVFPQ_OK:
+        msg = lib().ivfpq_last_error().decode(errors="replace")
+        raise IVFPQError(fn, status, msg)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream(stream=None):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return C.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _need(t, dtype, name, ndim=None, device=True):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if device and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# ---------------------------------------------------------------------------
+class Index:
+    """Owner of an ivfpq_index handle."""
+
+    def __init__(self, handle, d, nlist, m):
+        self.handle = handle
+        self.d, self.nlist, self.m = d, nlist, m
+
+    def __del__(self):
+        try:
+            if self.handle:
+                lib().ivfpq_index_destroy(self.handle)
+                self.handle = None
+        except Exception:
+            pass
+
+    @property
+    def ntotal(self):
+        return int(lib().ivfpq_ntotal(self.handle))
+
+
+def ivfpq_index_create(centroids, codebooks, nbits=8):
+    """centroids: fp32 [nlist, d]; codebooks: fp32 [m, 256, d/m] (CUDA)."""
+    torch = _torch()
+    _need(centroids, torch.float32, "centroids", 2)
+    _need(codebooks, torch.float32, "codebooks", 3)
+    nlist, d = centroids.shape
+    m = codebooks.shape[0]
+    h = C.c_void_p()
+    _check("ivfpq_index_create",
+           lib().ivfpq_index_create(d, nlist, m, nbits, _ptr(centroids), _ptr(codebooks),
+                                    C.byref(h)))
+    return Index(h, d, nlist, m)
+
+
+def ivfpq_index_destroy(index):
+    if index.handle:
+        _check("ivfpq_index_destroy", lib().ivfpq_index_destroy(index.handle))
+        index.handle = None
+
+
+def ivfpq_set_lut_type(index, lut_type):
+    if isinstance(lut_type, str):
+        lut_type = LUT_TYPES[lut_type]
+    _check("ivfpq_set_lut_type", lib().ivfpq_set_lut_type(index.handle, int(lut_type)))
+
+
+def ivfpq_add(index, codes, list_ids, ids, stream=None):
+    """codes: uint8 [n, m]; list_ids: int32 [n]; ids: int64 [n] (CUDA)."""
+    torch = _torch()
+    _need(codes, torch.uint8, "codes", 2)
+    _need(list_ids, torch.int32, "list_ids", 1)
+    _need(ids, torch.int64, "ids", 1)
+    n = codes.shape[0]
+    if codes.shape[1] != index.m or list_ids.shape[0] != n or ids.shape[0] != n:
+        raise ValueError("ivfpq_add: inconsistent shapes")
+    _check("ivfpq_add", lib().ivfpq_add(index.handle, _ptr(codes), _ptr(list_ids), _ptr(ids), n,
+                                         _stream(stream)))
+
+
+def ivfpq_search(index, queries, nprobe, k, out_dist=None, out_ids=None, stream=None):
+    torch = _torch()
+    _need(queries, torch.float32, "queries", 2)
+    nq = queries.shape[0]
+    if queries.shape[1] != index.d:
+        raise ValueError("ivfpq_search: query dimension mismatch")
+    if out_dist is None:
+        out_dist = torch.empty((nq, k), dtype=torch.float32, device=queries.device)
+    if out_ids is None:
+        out_ids = torch.empty((nq, k), dtype=torch.int64, device=queries.device)
+    _need(out_dist, torch.float32, "out_dist", 2)
+    _need(out_ids, torch.int64, "out_ids", 2)
+    _check("ivfpq_search", lib().ivfpq_search(index.handle, _ptr(queries), nq, nprobe, k,
+                                               _ptr(out_dist), _ptr(out_ids), _stream(stream)))
+    return out_dist, out_ids
+
+
+def ivfpq_search_probes(index, queries, nprobe, with_dist=True, stream=None):
+    torch = _torch()
+    _need(queries, torch.float32, "queries", 2)
+    nq = queries.shape[0]
+    probes = torch.empty((nq, nprobe), dtype=torch.int32, device=queries.device)
+    coarse = (torch.empty((nq, nprobe), dtype=torch.float32, device=queries.device)
+              if with_dist else None)
+    _check("ivfpq_search_probes",
+           lib().ivfpq_search_probes(index.handle, _ptr(queries), nq, nprobe, _ptr(probes),
+                                     _ptr(coarse), _stream(stream)))
+    return probes, coarse
+
+
+def ivfpq_search_preassigned(index, queries, probes, k, out_dist=None, out_ids=None,
+                             stream=None):
+    torch = _torch()
+    _need(queries, torch.float32, "queries", 2)
+    _need(probes, torch.int32, "probes", 2)
+    nq, nprobe = probes.shape
+    if out_dist is None:
+        out_dist = torch.empty((nq, k), dtype=torch.float32, device=queries.device)
+    if out_ids is None:
+        out_ids = torch.empty((nq, k), dtype=torch.int64, device=queries.device)
+    _check("ivfpq_search_preassigned",
+           lib().ivfpq_search_preassigned(index.handle, _ptr(queries), nq, nprobe, _ptr(probes), k,
+                                          _ptr(out_dist), _ptr(out_ids), _stream(stream)))
+    return out_dist, out_ids
+
+
+def ivfpq_set_profiling(index, enable=True):
+    _check("ivfpq_set_profiling", lib().ivfpq_set_profiling(index.handle, int(bool(enable))))
+
+
+def ivfpq_stage_times(index):
+    """[coarse, plan, scan, merge] milliseconds of the last search."""
+    buf = (C.c_float * 4)()
+    _check("ivfpq_stage_times", lib().ivfpq_stage_times(index.handle, buf))
+    return list(buf)
+
+
+def flat_knn(db, queries, k, out_dist=None, out_ids=None, stream=None):
+    torch = _torch()
+    _need(db, torch.float32, "db", 2)
+    _need(queries, torch.float32, "queries", 2)
+    n, d = db.shape
+    nq = queries.shape[0]
+    if queries.shape[1] != d:
+        raise ValueError("flat_knn: dimension mismatch")
+    if out_dist is None:
+        out_dist = torch.empty((nq, k), dtype=torch.float32, device=queries.device)
+    if out_ids is None:
+        out_ids = torch.empty((nq, k), dtype=torch.int64, device=queries.device)
+    _check("flat_knn", lib().flat_knn(_ptr(db), n, d, _ptr(queries), nq, k, _ptr(out_dist),
+                                       _ptr(out_ids), _stream(stream)))
+    return out_dist, out_ids
+
+
+def kselect(vals, k, out_vals=None, out_idx=None, stream=None):
+    torch = _torch()
+    _need(vals, torch.float32, "vals", 2)
+    rows, cols = vals.shape
+    if out_vals is None:
+        out_vals = torch.empty((rows, k), dtype=torch.float32, device=vals.device)
+    if out_idx is None:
+        out_idx = torch.empty((rows, k), dtype=torch.int64, device=vals.device)
+    _check("kselect", lib().kselect(_ptr(vals), rows, cols, k, _ptr(out_vals), _ptr(out_idx),
+                                     _stream(stream)))
+    return out_vals, out_idx

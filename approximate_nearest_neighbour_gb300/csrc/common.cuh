@@ -1,0 +1,122 @@
+// Shared host/device helpers of libivfpq_gb300: status handling, the
+// thread-local error message, workspace allocation and small device utilities.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "ivfpq.h"
+
+namespace ivfpq {
+
+// ---- error reporting --------------------------------------------------------
+void set_error(const char* fmt, ...);
+void clear_error();
+
+#define IVFPQ_REQUIRE(cond, ...)                   \
+  do {                                             \
+    if (!(cond)) {                                 \
+      ::ivfpq::set_error(__VA_ARGS__);             \
+      return IVFPQ_ERR_INVALID_ARG;                \
+    }                                              \
+  } while (0)
+
+#define IVFPQ_CUDA(expr)                                                        \
+  do {                                                                          \
+    cudaError_t e_ = (expr);                                                    \
+    if (e_ != cudaSuccess) {                                                    \
+      ::ivfpq::set_error("%s failed: %s (%s:%d)", #expr, cudaGetErrorString(e_), \
+                         __FILE__, __LINE__);                                   \
+      return e_ == cudaErrorMemoryAllocation ? IVFPQ_ERR_OOM : IVFPQ_ERR_CUDA;  \
+    }                                                                           \
+  } while (0)
+
+#define IVFPQ_TRY(expr)              \
+  do {                               \
+    int s_ = (expr);                 \
+    if (s_ != IVFPQ_OK) return s_;   \
+  } while (0)
+
+// Checks the launch that was just enqueued.
+#define IVFPQ_LAUNCHED() IVFPQ_CUDA(cudaGetLastError())
+
+// ---- stream-ordered workspace --------------------------------------------------
+// Frees its allocations on the stream (stream-ordered) when it goes out of
+// scope, so a failing call never leaks workspace.
+class Workspace {
+ public:
+  explicit Workspace(cudaStream_t s) : s_(s) {}
+  ~Workspace() {
+    for (int i = 0; i < n_; ++i) cudaFreeAsync(p_[i], s_);
+  }
+  template <class T>
+  int alloc(T** out, size_t count) {
+    *out = nullptr;
+    if (count == 0) return IVFPQ_OK;
+    if (n_ == kMax) {
+      set_error("internal: too many workspace buffers");
+      return IVFPQ_ERR_CUDA;
+    }
+    void* p = nullptr;
+    cudaError_t e = cudaMallocAsync(&p, count * sizeof(T), s_);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      set_error("workspace allocation of %zu bytes failed: %s", count * sizeof(T),
+                cudaGetErrorString(e));
+      return IVFPQ_ERR_OOM;
+    }
+    p_[n_++] = p;
+    *out = static_cast<T*>(p);
+    return IVFPQ_OK;
+  }
+
+ private:
+  static const int kMax = 16;
+  cudaStream_t s_;
+  void* p_[kMax];
+  int n_ = 0;
+};
+
+inline int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---- device utilities ---------------------------------------------------------
+constexpr unsigned kFullMask = 0xffffffffu;
+constexpr uint32_t kSentinelKey = 0xffffffffu;
+constexpr uint32_t kSentinelIdx = 0xffffffffu;
+
+// Order-preserving map from fp32 to uint32 (negative values flip all bits,
+// non-negative values flip the sign bit): a < b as floats iff key(a) < key(b)
+// as unsigned integers (with -0 ordered just below +0). +inf maps to
+// 0xff800000, below the sentinel key 0xffffffff.
+__device__ __forceinline__ uint32_t float_to_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  return u ^ (uint32_t(int32_t(u) >> 31) | 0x80000000u);
+}
+__device__ __forceinline__ float key_to_float(uint32_t k) {
+  if (k == kSentinelKey) return __int_as_float(0x7f800000);
+  return __uint_as_float(k ^ (uint32_t(int32_t(~k) >> 31) | 0x80000000u));
+}
+
+// Distances produced by the list scan are sums of non-negative terms, so
+// their raw fp32 bits already order correctly as unsigned integers; the
+// sentinel 0xffffffff lies above +inf (0x7f800000).
+__device__ __forceinline__ float dist_key_to_float(uint32_t k) {
+  return k == kSentinelKey ? __int_as_float(0x7f800000) : __uint_as_float(k);
+}
+
+}  // namespace ivfpq

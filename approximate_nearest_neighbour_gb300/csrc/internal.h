@@ -1,0 +1,81 @@
+// Internal host-side interfaces shared by the translation units of
+// libivfpq_gb300 (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "common.cuh"
+
+namespace ivfpq {
+
+// ---- k-selection launchers (select_k*.cu, kselect.cu) -------------------------
+enum class OutKind {
+  Float,    // fp32 value (from an order-preserving key) + int64 column index
+  Dist,     // fp32 distance (raw non-negative key) + int64 id looked up in id_map
+  Probes,   // int32 column index + optional fp32 value
+  Partial   // raw (key, index) pairs, k per (row, chunk)
+};
+
+struct SelectOut {
+  OutKind kind = OutKind::Float;
+  float* vals = nullptr;          // Float / Dist / Probes (optional)
+  int64_t* idx64 = nullptr;       // Float / Dist
+  int32_t* idx32 = nullptr;       // Probes
+  const int64_t* id_map = nullptr;  // Dist: slot -> id
+  uint32_t* pkeys = nullptr;      // Partial: [rows][chunks][k]
+  uint32_t* pidx = nullptr;
+};
+
+// Rows of fp32 values: row r holds vals[r*cols .. r*cols+cols). The columns of
+// each row are split into `chunks` ranges of `chunk_len` (chunks > 1 only
+// with OutKind::Partial). K = power of two >= max(32, k).
+int select_rows(const float* vals, int64_t rows, int64_t cols, int k, int64_t chunks,
+                int64_t chunk_len, const SelectOut& out, cudaStream_t s);
+
+// Rows of (key, index) pairs of length len: keys[r*len + i], idx[r*len + i].
+int select_pairs(const uint32_t* keys, const uint32_t* idx, int64_t rows, int64_t len, int k,
+                 int64_t chunks, int64_t chunk_len, const SelectOut& out, cudaStream_t s);
+
+// Two-level selection over long rows when there are few rows: a first pass
+// per column chunk into workspace, then a pass over the chunk winners.
+int kselect_device(const float* vals, int64_t rows, int64_t cols, int k, const SelectOut& out,
+                   cudaStream_t s);
+
+// ---- squared-L2 distance tiles (distance.cu) -----------------------------------
+// D[i*ldd + j] = sum_t (Q[i*d + t] - X[j*d + t])^2 for i < nq, j < n.
+int l2_distance_tile(const float* Q, int64_t nq, const float* X, int64_t n, int d, float* D,
+                     int64_t ldd, cudaStream_t s);
+
+// ---- flat / coarse search on distance tiles (flat.cu) ----------------------------
+// k nearest rows of X for each row of Q under squared L2; output as SelectOut
+// (Float with column ids, or Probes).
+int knn_by_tiles(const float* Q, int64_t nq, const float* X, int64_t n, int d, int k,
+                 const SelectOut& out, cudaStream_t s);
+
+}  // namespace ivfpq
+
+// ---- the index -------------------------------------------------------------------------
+struct ivfpq_index {
+  int d = 0, nlist = 0, m = 0, nbits = 8, dsub = 0;
+  int lut_type = IVFPQ_LUT_FP32;
+  int device = 0;
+  float* centroids = nullptr;   // [nlist, d]
+  float* cent_norms = nullptr;  // [nlist]
+  float* codebooks = nullptr;   // [m, 256, dsub]
+  // inverted lists, interleaved in blocks of 32 vectors
+  int64_t ntotal = 0;
+  int64_t nblocks = 0;
+  int32_t* list_len = nullptr;        // [nlist]
+  int64_t* list_block_off = nullptr;  // [nlist + 1], in blocks
+  uint8_t* codes = nullptr;           // [nblocks, 32 * m]
+  int64_t* ids = nullptr;             // [nblocks * 32], -1 on padding slots
+  std::vector<int64_t> h_list_len;    // host mirror of list_len
+  int64_t max_list_len = 0;
+  // optional per-stage timing
+  bool profile = false;
+  cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+  bool ev_recorded[5] = {false, false, false, false, false};
+};

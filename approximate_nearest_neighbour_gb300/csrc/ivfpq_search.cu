@@ -1,0 +1,229 @@
+// Batched IVF-PQ search: coarse quantizer, fused table build + list scan +
+// per-chunk selection, and the cross-chunk merge with id translation.
+//
+// Source: IVFPQ search steps 1-5 ("Custom 8-bit floating point value format
+// for reducing shared memory bank conflict in approximate nearest neighbor
+// search"); section 5 of "Billion-scale similarity search with GPUs" (tables
+// per query x list, queries x lists processed independently, two-pass
+// k-selection with subdivision factor f: here f = the number of list chunks
+// per query).
+#include <algorithm>
+
+#include "internal.h"
+#include "scan.cuh"
+
+namespace ivfpq {
+
+#define IVFPQ_EXTERN_SCAN(MW, K) \
+  extern template int launch_scan_mw<MW, K>(const ScanParams&, int64_t, cudaStream_t);
+#define IVFPQ_EXTERN_SCAN_ALL(K) \
+  IVFPQ_EXTERN_SCAN(0, K) IVFPQ_EXTERN_SCAN(2, K) IVFPQ_EXTERN_SCAN(4, K) IVFPQ_EXTERN_SCAN(8, K)
+IVFPQ_EXTERN_SCAN_ALL(32)
+IVFPQ_EXTERN_SCAN_ALL(64)
+IVFPQ_EXTERN_SCAN_ALL(128)
+IVFPQ_EXTERN_SCAN_ALL(256)
+IVFPQ_EXTERN_SCAN_ALL(512)
+IVFPQ_EXTERN_SCAN_ALL(1024)
+IVFPQ_EXTERN_SCAN_ALL(2048)
+IVFPQ_EXTERN_SCAN(16, 32)
+IVFPQ_EXTERN_SCAN(16, 64)
+IVFPQ_EXTERN_SCAN(16, 128)
+IVFPQ_EXTERN_SCAN(16, 256)
+
+// Code words per vector as a template argument where a specialised kernel
+// exists (m = 8, 16, 32; m = 64 for K <= 256); 0 selects the generic kernel.
+template <int K>
+int launch_scan_k(const ScanParams& p, int64_t nq, cudaStream_t s) {
+  switch (p.m) {
+    case 8: return launch_scan_mw<2, K>(p, nq, s);
+    case 16: return launch_scan_mw<4, K>(p, nq, s);
+    case 32: return launch_scan_mw<8, K>(p, nq, s);
+    case 64:
+      if constexpr (K <= 256) return launch_scan_mw<16, K>(p, nq, s);
+      else return launch_scan_mw<0, K>(p, nq, s);
+    default: return launch_scan_mw<0, K>(p, nq, s);
+  }
+}
+
+namespace {
+
+int queue_len(int k) {
+  int K = 32;
+  while (K < k) K *= 2;
+  return K;
+}
+
+int launch_scan(const ScanParams& p, int64_t nq, cudaStream_t s) {
+  switch (queue_len(p.k)) {
+    case 32: return launch_scan_k<32>(p, nq, s);
+    case 64: return launch_scan_k<64>(p, nq, s);
+    case 128: return launch_scan_k<128>(p, nq, s);
+    case 256: return launch_scan_k<256>(p, nq, s);
+    case 512: return launch_scan_k<512>(p, nq, s);
+    case 1024: return launch_scan_k<1024>(p, nq, s);
+    case 2048: return launch_scan_k<2048>(p, nq, s);
+  }
+  set_error("k=%d above %d", p.k, IVFPQ_MAX_K);
+  return IVFPQ_ERR_INVALID_ARG;
+}
+
+void record(const ivfpq_index* ix, int i, cudaStream_t s) {
+  auto* mix = const_cast<ivfpq_index*>(ix);
+  if (!mix->profile) return;
+  if (!mix->ev[i]) cudaEventCreate(&mix->ev[i]);
+  cudaEventRecord(mix->ev[i], s);
+  mix->ev_recorded[i] = true;
+}
+
+int coarse_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int nprobe,
+                 int32_t* probes, float* coarse, cudaStream_t s) {
+  SelectOut o;
+  o.kind = OutKind::Probes;
+  o.idx32 = probes;
+  o.vals = coarse;
+  return knn_by_tiles(queries, nq, ix->centroids, ix->nlist, ix->d, nprobe, o, s);
+}
+
+// Lists per block: enough blocks to give every SM several waves.
+void plan_chunks(int64_t nq, int nprobe, int* per_chunk, int* nchunks) {
+  const int64_t target = int64_t(num_sms()) * 3 * 8;
+  int64_t c = std::max<int64_t>(1, std::min<int64_t>(nprobe, ceil_div(target, std::max<int64_t>(nq, 1))));
+  int pc = int(ceil_div(nprobe, c));
+  *per_chunk = pc;
+  *nchunks = int(ceil_div(nprobe, pc));
+}
+
+int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int nprobe,
+               const int32_t* probes, int k, float* out_dist, int64_t* out_ids, cudaStream_t s) {
+  if (ix->lut_type != IVFPQ_LUT_FP32) {
+    set_error("lookup-table type %d is not available in this build of the scan", ix->lut_type);
+    return IVFPQ_ERR_UNSUPPORTED;
+  }
+  ScanParams p;
+  p.queries = queries;
+  p.centroids = ix->centroids;
+  p.codebooks_t = ix->codebooks;
+  p.probes = probes;
+  p.list_len = ix->list_len;
+  p.list_block_off = ix->list_block_off;
+  p.codes = ix->codes;
+  p.d = ix->d;
+  p.m = ix->m;
+  p.dsub = ix->dsub;
+  p.nlist = ix->nlist;
+  p.nprobe = nprobe;
+  p.k = k;
+  plan_chunks(nq, nprobe, &p.per_chunk, &p.nchunks);
+  Workspace ws(s);
+  const size_t np = size_t(nq) * p.nchunks * k;
+  IVFPQ_TRY(ws.alloc(&p.pkeys, np));
+  IVFPQ_TRY(ws.alloc(&p.pidx, np));
+  record(ix, 2, s);
+  IVFPQ_TRY(launch_scan(p, nq, s));
+  record(ix, 3, s);
+  SelectOut o;
+  o.kind = OutKind::Dist;
+  o.vals = out_dist;
+  o.idx64 = out_ids;
+  o.id_map = ix->ids;
+  const int64_t len = int64_t(p.nchunks) * k;
+  IVFPQ_TRY(select_pairs(p.pkeys, p.pidx, nq, len, k, 1, len, o, s));
+  record(ix, 4, s);
+  return IVFPQ_OK;
+}
+
+int check_common(const ivfpq_index* ix, const float* queries, int64_t nq, int nprobe,
+                 const char* who) {
+  IVFPQ_REQUIRE(ix, "%s: null index", who);
+  IVFPQ_REQUIRE(nq >= 0, "%s: negative nq", who);
+  IVFPQ_REQUIRE(nq < (int64_t(1) << 31), "%s: nq=%lld too large", who, (long long)nq);
+  IVFPQ_REQUIRE(nprobe >= 1 && nprobe <= ix->nlist && nprobe <= IVFPQ_MAX_K,
+                "%s: nprobe=%d outside [1, min(nlist=%d, %d)]", who, nprobe, ix->nlist,
+                IVFPQ_MAX_K);
+  IVFPQ_REQUIRE(queries || nq == 0, "%s: null queries", who);
+  return IVFPQ_OK;
+}
+
+void reset_events(const ivfpq_index* ix) {
+  auto* mix = const_cast<ivfpq_index*>(ix);
+  for (bool& r : mix->ev_recorded) r = false;
+}
+
+}  // namespace
+}  // namespace ivfpq
+
+using namespace ivfpq;
+
+extern "C" int ivfpq_search(const ivfpq_index* ix, const float* queries, int64_t nq, int nprobe,
+                            int k, float* out_dist, int64_t* out_ids, void* stream) {
+  clear_error();
+  IVFPQ_TRY(check_common(ix, queries, nq, nprobe, "ivfpq_search"));
+  IVFPQ_REQUIRE(k >= 1 && k <= IVFPQ_MAX_K, "ivfpq_search: k=%d outside [1, %d]", k, IVFPQ_MAX_K);
+  if (nq == 0) return IVFPQ_OK;
+  IVFPQ_REQUIRE(out_dist && out_ids, "ivfpq_search: null output");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  reset_events(ix);
+  Workspace ws(s);
+  int32_t* probes;
+  IVFPQ_TRY(ws.alloc(&probes, size_t(nq) * nprobe));
+  record(ix, 0, s);
+  IVFPQ_TRY(coarse_stage(ix, queries, nq, nprobe, probes, nullptr, s));
+  record(ix, 1, s);
+  return scan_stage(ix, queries, nq, nprobe, probes, k, out_dist, out_ids, s);
+}
+
+extern "C" int ivfpq_search_probes(const ivfpq_index* ix, const float* queries, int64_t nq,
+                                   int nprobe, int32_t* out_probes, float* out_coarse,
+                                   void* stream) {
+  clear_error();
+  IVFPQ_TRY(check_common(ix, queries, nq, nprobe, "ivfpq_search_probes"));
+  if (nq == 0) return IVFPQ_OK;
+  IVFPQ_REQUIRE(out_probes, "ivfpq_search_probes: null output");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  reset_events(ix);
+  record(ix, 0, s);
+  IVFPQ_TRY(coarse_stage(ix, queries, nq, nprobe, out_probes, out_coarse, s));
+  record(ix, 1, s);
+  return IVFPQ_OK;
+}
+
+extern "C" int ivfpq_search_preassigned(const ivfpq_index* ix, const float* queries, int64_t nq,
+                                        int nprobe, const int32_t* probes, int k,
+                                        float* out_dist, int64_t* out_ids, void* stream) {
+  clear_error();
+  IVFPQ_REQUIRE(ix, "ivfpq_search_preassigned: null index");
+  IVFPQ_REQUIRE(nq >= 0 && nq < (int64_t(1) << 31), "ivfpq_search_preassigned: bad nq");
+  IVFPQ_REQUIRE(nprobe >= 1 && nprobe <= (1 << 20), "ivfpq_search_preassigned: bad nprobe=%d",
+                nprobe);
+  IVFPQ_REQUIRE(k >= 1 && k <= IVFPQ_MAX_K, "ivfpq_search_preassigned: k=%d outside [1, %d]", k,
+                IVFPQ_MAX_K);
+  if (nq == 0) return IVFPQ_OK;
+  IVFPQ_REQUIRE(queries && probes && out_dist && out_ids, "ivfpq_search_preassigned: null pointer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  reset_events(ix);
+  return scan_stage(ix, queries, nq, nprobe, probes, k, out_dist, out_ids, s);
+}
+
+extern "C" int ivfpq_set_profiling(ivfpq_index* ix, int enable) {
+  clear_error();
+  IVFPQ_REQUIRE(ix, "ivfpq_set_profiling: null index");
+  ix->profile = enable != 0;
+  return IVFPQ_OK;
+}
+
+extern "C" int ivfpq_stage_times(const ivfpq_index* ix, float* ms) {
+  clear_error();
+  IVFPQ_REQUIRE(ix && ms, "ivfpq_stage_times: null pointer");
+  for (int i = 0; i < 4; ++i) ms[i] = 0.f;
+  // stage i spans events (i, i+1); the planning stage has no events of its own
+  const int pairs[4][2] = {{0, 1}, {1, 2}, {2, 3}, {3, 4}};
+  for (int i = 0; i < 4; ++i) {
+    const int a = pairs[i][0], b = pairs[i][1];
+    if (!ix->ev_recorded[a] || !ix->ev_recorded[b]) continue;
+    IVFPQ_CUDA(cudaEventSynchronize(ix->ev[b]));
+    float t = 0.f;
+    IVFPQ_CUDA(cudaEventElapsedTime(&t, ix->ev[a], ix->ev[b]));
+    ms[i] = t;
+  }
+  return IVFPQ_OK;
+}

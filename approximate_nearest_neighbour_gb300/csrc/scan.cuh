@@ -1,0 +1,251 @@
+// Fused ADC lookup-table build, inverted-list scan and per-chunk k-selection.
+//
+// Source: "Billion-scale similarity search with GPUs", section 5 -- the
+// tables T_1..T_b of 256 entries per sub-quantizer (a distance is b look-ups
+// and additions), the tables kept in shared memory, queries x lists processed
+// independently, and the two-pass k-selection (k results per chunk of lists,
+// then a final k-selection); "Custom 8-bit floating point value format ...",
+// search steps 2-5 and Eq. (1): residual r = q - c, F(y_j) = ||r_j - codeword||^2,
+// R = sum_j F(y_j).
+//
+// One thread block handles one query and a chunk of `per_chunk` of its probed
+// lists. For each list it forms the residual, builds all m tables in shared
+// memory, and its 8 warps scan the list's 32-vector blocks (warp w takes
+// blocks w, w+8, ...); lane i of a warp computes the distance of the vector in
+// slot i and inserts it into the warp's WarpSelect. The warp queues survive
+// across the chunk's lists; at the end they are merged (BlockSelect) and the
+// chunk's k best (distance, slot) pairs are written out.
+//
+// Shared-memory table layout (fp32): tables are grouped by 32; a group is a
+// 256 x 64 array of 4-byte words, row e = reproduction value, and column c
+// holds the table of sub-quantizer 32g + (c mod gs). At step s of a group,
+// lane i reads column i + s of row code_byte. Word (e, c) sits in bank
+// (64 e + c) mod 32 = c mod 32, and i + s takes 32 distinct values mod 32
+// across the warp, so every look-up instruction is free of bank conflicts
+// whatever the code bytes are. (A plain table per sub-quantizer, entry e in
+// word e, gives up to 7 conflicts per look-up in fp32 and 3 in fp16, as the
+// 8-bit-float page computes.) The code bytes are stored pre-rotated
+// (layout.cuh) so that the byte lane i needs at step s is simply stored byte s.
+#pragma once
+
+#include "internal.h"
+#include "layout.cuh"
+#include "select.cuh"
+
+namespace ivfpq {
+
+struct ScanParams {
+  const float* queries;      // [nq, d]
+  const float* centroids;    // [nlist, d]
+  const float* codebooks_t;  // [256, m, dsub]
+  const int32_t* probes;     // [nq, nprobe]
+  const int32_t* list_len;   // [nlist]
+  const int64_t* list_block_off;  // [nlist + 1]
+  const uint8_t* codes;      // blocks of 32 * m bytes
+  uint32_t* pkeys;           // [nq, nchunks, k]
+  uint32_t* pidx;
+  int d, m, dsub, nlist, nprobe, per_chunk, nchunks, k;
+};
+
+constexpr int kScanWarps = 8;
+constexpr int kGroupWords = 256 * 64;  // one group of up to 32 tables
+
+inline size_t scan_smem_bytes(int m, int d, int K) {
+  const size_t lut = size_t((m + 31) / 32) * kGroupWords * 4;
+  const size_t merge = size_t(kScanWarps) * K * 8;
+  return (lut > merge ? lut : merge) + size_t((d + 3) / 4) * 16;
+}
+
+__device__ __forceinline__ uint4 ld_code16(const uint8_t* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ uint2 ld_code8(const uint8_t* p) {
+  return __ldcs(reinterpret_cast<const uint2*>(p));
+}
+__device__ __forceinline__ uint32_t ld_code4(const uint8_t* p) {
+  return __ldcs(reinterpret_cast<const unsigned int*>(p));
+}
+
+// Stored code words of slot `lane` in a block (MW = m / 4 words).
+template <int MW>
+__device__ __forceinline__ void load_codes(const uint8_t* blk, int lane, uint32_t (&w)[MW]) {
+  constexpr int NF = MW / 4, RW = MW % 4;
+#pragma unroll
+  for (int c = 0; c < NF; ++c) {
+    const uint4 v = ld_code16(blk + c * 512 + lane * 16);
+    w[4 * c] = v.x;
+    w[4 * c + 1] = v.y;
+    w[4 * c + 2] = v.z;
+    w[4 * c + 3] = v.w;
+  }
+  const uint8_t* rp = blk + NF * 512 + lane * (4 * RW);
+  if (RW == 1) {
+    w[4 * NF] = ld_code4(rp);
+  } else if (RW == 2) {
+    const uint2 v = ld_code8(rp);
+    w[4 * NF] = v.x;
+    w[4 * NF + 1] = v.y;
+  } else if (RW == 3) {
+    w[4 * NF] = ld_code4(rp);
+    w[4 * NF + 1] = ld_code4(rp + 4);
+    w[4 * NF + 2] = ld_code4(rp + 8);
+  }
+}
+
+// Sum of the m table entries selected by the stored code words.
+template <int MW>
+__device__ __forceinline__ float adc_sum(const uint32_t (&w)[MW], const float* lut_lane) {
+  float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+  for (int s = 0; s < 4 * MW; ++s) {
+    const uint32_t byte = (w[s >> 2] >> (8 * (s & 3))) & 0xffu;
+    const float v = lut_lane[(s >> 5) * kGroupWords + int(byte) * 64 + (s & 31)];
+    if (s & 1)
+      acc1 += v;
+    else
+      acc0 += v;
+  }
+  return acc0 + acc1;
+}
+
+// All m tables of residual r (shared memory, d floats) into `lut`.
+__device__ __forceinline__ void build_lut(float* lut, const float* r, const float* cbt, int m,
+                                          int dsub, int warp, int lane) {
+  const int ngroups = (m + 31) >> 5;
+  for (int g = 0; g < ngroups; ++g) {
+    const int gs = group_size(g, m);
+    float* base = lut + g * kGroupWords;
+    if ((gs & (gs - 1)) == 0) {
+      // Each (table, value) pair computed once, then stored to its 64/gs
+      // columns; lane i starts at a different copy so the stores of one
+      // instruction fall into 32 distinct banks.
+      const int reps = 64 / gs;
+      const int jj = lane % gs, qq = lane / gs;
+      const int j = 32 * g + jj;
+      const float* rj = r + j * dsub;
+      for (int it = warp * 32; it < 256 * gs; it += kScanWarps * 32) {
+        const int e = (it + lane) / gs;
+        const float* c = cbt + (int64_t(e) * m + j) * dsub;
+        float T = 0.f;
+        for (int t = 0; t < dsub; ++t) {
+          const float diff = rj[t] - __ldg(c + t);
+          T = fmaf(diff, diff, T);
+        }
+        float* row = base + e * 64 + jj;
+        for (int s = 0; s < reps; ++s) row[gs * ((s + qq) % reps)] = T;
+      }
+    } else {
+      for (int it = warp * 32 + lane; it < kGroupWords; it += kScanWarps * 32) {
+        const int e = it >> 6, col = it & 63;
+        const int j = 32 * g + col % gs;
+        const float* c = cbt + (int64_t(e) * m + j) * dsub;
+        const float* rj = r + j * dsub;
+        float T = 0.f;
+        for (int t = 0; t < dsub; ++t) {
+          const float diff = rj[t] - __ldg(c + t);
+          T = fmaf(diff, diff, T);
+        }
+        base[it] = T;
+      }
+    }
+  }
+}
+
+template <int MW, int K>
+__global__ void __launch_bounds__(kScanWarps * 32)
+ivfpq_scan_kernel(const ScanParams p) {
+  constexpr int T = ThreadQ<K>::value;
+  constexpr int NW = kScanWarps;
+  extern __shared__ __align__(16) uint32_t scan_smem[];
+  const int m = MW > 0 ? 4 * MW : p.m;
+  const int ngroups = (m + 31) >> 5;
+  float* lut = reinterpret_cast<float*>(scan_smem);
+  const int lut_words = ngroups * kGroupWords;
+  const int merge_words = NW * K * 2;
+  float* res = reinterpret_cast<float*>(scan_smem) + (lut_words > merge_words ? lut_words : merge_words);
+
+  const int64_t q = int64_t(blockIdx.x) / p.nchunks;
+  const int chunk = int(int64_t(blockIdx.x) % p.nchunks);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  WarpSelect<K, T> ws;
+  ws.init(lane);
+  const int p0 = chunk * p.per_chunk;
+  const int p1 = min(p.nprobe, p0 + p.per_chunk);
+  const float* lut_lane = lut + lane;
+
+  for (int pi = p0; pi < p1; ++pi) {
+    const int l = p.probes[q * p.nprobe + pi];
+    if (l < 0 || l >= p.nlist) continue;  // same value for the whole block
+    __syncthreads();  // the previous list's scan no longer reads the tables
+    for (int t = tid; t < p.d; t += NW * 32)
+      res[t] = p.queries[q * p.d + t] - p.centroids[int64_t(l) * p.d + t];
+    __syncthreads();
+    build_lut(lut, res, p.codebooks_t, m, p.dsub, warp, lane);
+    __syncthreads();
+    const int len = p.list_len[l];
+    const int64_t boff = p.list_block_off[l];
+    const int nb = (len + 31) >> 5;
+    const uint8_t* lcodes = p.codes + boff * 32 * m;
+    if constexpr (MW > 0) {
+      uint32_t cur[MW], nxt[MW];
+      int b = warp;
+      if (b < nb) load_codes<MW>(lcodes + int64_t(b) * 32 * m, lane, cur);
+      for (; b < nb; b += NW) {
+        const int bn = b + NW;
+        if (bn < nb) load_codes<MW>(lcodes + int64_t(bn) * 32 * m, lane, nxt);
+        const float dist = adc_sum<MW>(cur, lut_lane);
+        const bool valid = b * 32 + lane < len;
+        ws.add(valid ? __float_as_uint(dist) : kSentinelKey, uint32_t((boff + b) * 32 + lane));
+#pragma unroll
+        for (int w = 0; w < MW; ++w) cur[w] = nxt[w];
+      }
+    } else {
+      for (int b = warp; b < nb; b += NW) {
+        const uint8_t* blk = lcodes + int64_t(b) * 32 * m;
+        float dist = 0.f;
+        for (int s0 = 0; s0 < m; s0 += 4) {
+          const uint32_t word =
+              *reinterpret_cast<const uint32_t*>(blk + stored_byte_offset(lane, s0, m));
+#pragma unroll
+          for (int bb = 0; bb < 4; ++bb) {
+            const int s = s0 + bb;
+            const uint32_t byte = (word >> (8 * bb)) & 0xffu;
+            dist += lut_lane[(s >> 5) * kGroupWords + int(byte) * 64 + (s & 31)];
+          }
+        }
+        const bool valid = b * 32 + lane < len;
+        ws.add(valid ? __float_as_uint(dist) : kSentinelKey, uint32_t((boff + b) * 32 + lane));
+      }
+    }
+  }
+  ws.finalize();
+  __syncthreads();  // the table area is reused for the block merge
+  block_merge<K, T, NW>(ws, scan_smem, scan_smem + NW * K, warp);
+  if (warp == 0) {
+    const int64_t o = (q * p.nchunks + chunk) * p.k;
+#pragma unroll
+    for (int r = 0; r < K / 32; ++r) {
+      const int i = 32 * r + lane;
+      if (i < p.k) {
+        p.pkeys[o + i] = ws.wk[r];
+        p.pidx[o + i] = ws.wv[r];
+      }
+    }
+  }
+}
+
+template <int MW, int K>
+int launch_scan_mw(const ScanParams& p, int64_t nq, cudaStream_t s) {
+  auto kern = ivfpq_scan_kernel<MW, K>;
+  const size_t smem = scan_smem_bytes(p.m, p.d, K);
+  IVFPQ_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+  const int64_t blocks = nq * p.nchunks;
+  kern<<<unsigned(blocks), kScanWarps * 32, smem, s>>>(p);
+  IVFPQ_LAUNCHED();
+  return IVFPQ_OK;
+}
+
+}  // namespace ivfpq
+
+#define IVFPQ_INST_SCAN(MW, K) \
+  template int ivfpq::launch_scan_mw<MW, K>(const ivfpq::ScanParams&, int64_t, cudaStream_t);

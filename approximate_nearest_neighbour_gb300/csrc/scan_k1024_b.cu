@@ -1,0 +1,6 @@
+// IVF-PQ list-scan kernel instantiations (split across files to keep
+// compile units small).
+#include "scan.cuh"
+
+IVFPQ_INST_SCAN(4, 1024)
+IVFPQ_INST_SCAN(8, 1024)

@@ -1,0 +1,5 @@
+// IVF-PQ list-scan kernel instantiations (split across files to keep
+// compile units small).
+#include "scan.cuh"
+
+IVFPQ_INST_SCAN(2, 2048)

@@ -1,0 +1,208 @@
+/*
+ * ivfpq.h -- C ABI of the GB300 (sm_103a) batched IVF-PQ search library
+ * (libivfpq_gb300.so).
+ *
+ * The library implements the search path of the method described in
+ * "Billion-scale similarity search with GPUs" (Johnson, Douze, Jegou): a
+ * coarse quantizer, per-(query, list) ADC lookup tables, a scan of the PQ codes
+ * in the probed inverted lists, and register-resident k-selection (WarpSelect /
+ * BlockSelect) merged across lists. Exact brute-force k-NN and stand-alone
+ * row-wise k-selection are exposed too.
+ *
+ * Conventions for every entry point:
+ *  - Array pointers are DEVICE pointers (for example torch tensors'
+ *    data_ptr()) unless stated otherwise; matrices are row-major and densely
+ *    packed. `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *  - Calls enqueue work on `stream` and return without synchronizing, except
+ *    ivfpq_add, which synchronizes `stream` once (it needs the new list sizes
+ *    on the host to size the list storage).
+ *  - Argument errors are detected on the host before any work is enqueued; in
+ *    that case nothing is written and IVFPQ_ERR_INVALID_ARG (or
+ *    IVFPQ_ERR_UNSUPPORTED) is returned. CUDA errors return IVFPQ_ERR_CUDA,
+ *    failed workspace allocations IVFPQ_ERR_OOM. ivfpq_last_error() gives a
+ *    message for the most recent failure on the calling thread.
+ *  - Distances are squared L2 distances. Results are ordered by ascending
+ *    distance; when fewer than k results exist the tail is (+inf, -1). The
+ *    order of equal distances is unspecified.
+ *  - Workspace is taken from the device's stream-ordered memory pool
+ *    (cudaMallocAsync) on `stream` and returned on the same stream.
+ *  - Search calls on one index may run concurrently on different streams;
+ *    ivfpq_add must not overlap a search of the same index.
+ */
+#ifndef IVFPQ_GB300_H
+#define IVFPQ_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ivfpq_index ivfpq_index; /* opaque; owned by the library */
+
+typedef enum {
+  IVFPQ_OK = 0,
+  IVFPQ_ERR_INVALID_ARG = -1,
+  IVFPQ_ERR_UNSUPPORTED = -2,
+  IVFPQ_ERR_OOM = -3,
+  IVFPQ_ERR_CUDA = -4,
+  IVFPQ_ERR_DEVICE_CHECK = -5,
+  IVFPQ_ERR_TIMEOUT = -6
+} ivfpq_status;
+
+/* Storage type of the ADC lookup tables built in shared memory. */
+typedef enum {
+  IVFPQ_LUT_FP32 = 0, /* IEEE binary32 */
+  IVFPQ_LUT_FP16 = 1, /* IEEE binary16, round to nearest even */
+  IVFPQ_LUT_FP8 = 2   /* 1 sign / 4 exponent / 3 mantissa bits (E4M3), one
+                         fp32 scale per table set */
+} ivfpq_lut_type;
+
+#define IVFPQ_MAX_K 2048  /* largest k accepted by every search entry point */
+#define IVFPQ_MAX_M 64    /* largest number of sub-quantizers */
+
+/*
+ * ivfpq_index_create -- an empty IVF-PQ index.
+ * Source: IVFADC ("Billion-scale similarity search with GPUs", section 5:
+ * coarse quantizer q1 with |C1| centroids, product quantizer with b
+ * sub-quantizers of 256 reproduction values each; b any multiple of 4 up to 64).
+ *  d          vector dimension, > 0, multiple of m
+ *  nlist      number of inverted lists / coarse centroids, 1 .. 2^24
+ *  m          number of sub-quantizers (bytes per code): a multiple of 4, <= 64
+ *  nbits      bits per sub-quantizer index; must be 8
+ *  centroids  device fp32 [nlist, d]
+ *  codebooks  device fp32 [m, 256, d/m]: codebooks[(j*256 + e)*(d/m) + t] is
+ *             dimension t of reproduction value e of sub-quantizer j, which
+ *             quantizes dimensions [j*d/m, (j+1)*d/m) of the residual
+ *  out        receives the handle
+ * The inputs are copied (synchronously, on the legacy default stream); the
+ * caller keeps ownership of them. Errors: INVALID_ARG, UNSUPPORTED (nbits != 8,
+ * m not a multiple of 4 or > 64), OOM, CUDA.
+ */
+int ivfpq_index_create(int d, int nlist, int m, int nbits, const float* centroids,
+                       const float* codebooks, ivfpq_index** out);
+
+/* ivfpq_index_destroy -- frees the index (synchronizes the device first).
+ * NULL is accepted. */
+int ivfpq_index_destroy(ivfpq_index* index);
+
+/*
+ * ivfpq_set_lut_type -- storage type of the lookup tables used by later
+ * searches (ivfpq_lut_type). Source: fp32 / fp16 tables ("Billion-scale
+ * similarity search with GPUs", section 5, the paragraph on T_i in shared
+ * memory); 8-bit float tables ("Custom 8-bit floating point value format for
+ * reducing shared memory bank conflict in approximate nearest neighbor
+ * search", title and the paragraph on the norm2 fragment lookup table).
+ * Errors: INVALID_ARG for an unknown type.
+ */
+int ivfpq_set_lut_type(ivfpq_index* index, int lut_type);
+
+/*
+ * ivfpq_add -- appends n encoded vectors to the inverted lists.
+ * Source: IVFPQ build step 4 ("Custom 8-bit floating point ..." page): store
+ * each vector's list and its PQ code; codes are kept as sequential groups of m
+ * bytes per vector within lists ("Billion-scale similarity search with GPUs",
+ * section 5). The library stores them interleaved in blocks of 32 vectors.
+ *  codes     device uint8 [n, m], row-major
+ *  list_ids  device int32 [n], each in [0, nlist)
+ *  ids       device int64 [n], the ids returned by searches
+ * Vectors keep their relative order inside each list (earlier rows first).
+ * The inputs are copied; they may be freed once `stream` has completed.
+ * Synchronizes `stream`. Errors: INVALID_ARG (also when a list id is out of
+ * range; then the index is unchanged), OOM, CUDA.
+ */
+int ivfpq_add(ivfpq_index* index, const uint8_t* codes, const int32_t* list_ids,
+              const int64_t* ids, int64_t n, void* stream);
+
+/* ivfpq_ntotal -- number of vectors stored (host value), or -1 for NULL. */
+int64_t ivfpq_ntotal(const ivfpq_index* index);
+
+/*
+ * ivfpq_search -- batched IVF-PQ search.
+ * Source: IVFPQ search steps 1-5 and Eq. (1) ("Custom 8-bit floating point
+ * ..." page); lookup tables T_1..T_b and their use in the list scan, two-pass
+ * k-selection ("Billion-scale similarity search with GPUs", section 5).
+ * For each query: the nprobe nearest centroids (ties to the lower list id),
+ * per probed list the table T_j[e] = ||r^(j) - codeword_j(e)||^2 of the
+ * residual r = query - centroid, the distance sum_j T_j[code_j] of every
+ * stored vector, and the k smallest over all probed lists.
+ *  queries   device fp32 [nq, d]
+ *  nprobe    1 .. nlist;  k  1 .. IVFPQ_MAX_K
+ *  out_dist  device fp32 [nq, k];  out_ids  device int64 [nq, k]
+ * Errors: INVALID_ARG, OOM, CUDA.
+ */
+int ivfpq_search(const ivfpq_index* index, const float* queries, int64_t nq, int nprobe,
+                 int k, float* out_dist, int64_t* out_ids, void* stream);
+
+/*
+ * ivfpq_search_probes -- the coarse-quantizer stage alone: for each query the
+ * nprobe nearest list ids (ascending distance, ties to the lower id) and their
+ * squared distances. Same source and argument rules as ivfpq_search.
+ *  out_probes  device int32 [nq, nprobe];  out_coarse  device fp32 [nq, nprobe]
+ *  (out_coarse may be NULL)
+ */
+int ivfpq_search_probes(const ivfpq_index* index, const float* queries, int64_t nq,
+                        int nprobe, int32_t* out_probes, float* out_coarse, void* stream);
+
+/*
+ * ivfpq_search_preassigned -- lookup-table build, list scan and k-selection
+ * for caller-given probes (the stages after the coarse quantizer).
+ *  probes  device int32 [nq, nprobe], each in [0, nlist); a list given twice
+ *          for one query contributes its vectors twice
+ * Other arguments as ivfpq_search.
+ */
+int ivfpq_search_preassigned(const ivfpq_index* index, const float* queries, int64_t nq,
+                             int nprobe, const int32_t* probes, int k, float* out_dist,
+                             int64_t* out_ids, void* stream);
+
+/*
+ * ivfpq_set_profiling / ivfpq_stage_times -- optional per-stage timing. When
+ * enabled, the search entry points record CUDA events on `stream` around each
+ * stage; after the stream has completed, ivfpq_stage_times writes the elapsed
+ * milliseconds of the most recent search into ms[0..3]:
+ * [0] coarse quantizer (distances + top-nprobe), [1] grouping / planning,
+ * [2] lookup tables + list scan + per-chunk selection, [3] cross-list merge.
+ * Stages that did not run report 0. Synchronizes on the last recorded event.
+ */
+int ivfpq_set_profiling(ivfpq_index* index, int enable);
+int ivfpq_stage_times(const ivfpq_index* index, float* ms);
+
+/*
+ * flat_knn -- exact brute-force k-NN under squared L2.
+ * Source: exact search by a GEMM-form distance ||x||^2 - 2<x, y> + ||y||^2
+ * followed by k-selection ("Billion-scale similarity search with GPUs",
+ * sections 4-5, "as with exact search").
+ *  db       device fp32 [n, d];  queries  device fp32 [nq, d]
+ *  k        1 .. IVFPQ_MAX_K
+ *  out_dist device fp32 [nq, k];  out_ids  device int64 [nq, k] (row index in db)
+ * Errors: INVALID_ARG, OOM, CUDA.
+ */
+int flat_knn(const float* db, int64_t n, int d, const float* queries, int64_t nq, int k,
+             float* out_dist, int64_t* out_ids, void* stream);
+
+/*
+ * kselect -- the k smallest values of each row with their column index.
+ * Source: WarpSelect ("Billion-scale similarity search with GPUs", section 4,
+ * Algorithm 3) with BlockSelect (several warps, queues merged in shared memory)
+ * for long rows.
+ *  vals      device fp32 [rows, cols]; +-inf allowed, NaN not supported
+ *  k         1 .. IVFPQ_MAX_K;  cols < 2^32 - 1
+ *  out_vals  device fp32 [rows, k];  out_idx  device int64 [rows, k]
+ * Errors: INVALID_ARG, OOM, CUDA.
+ */
+int kselect(const float* vals, int64_t rows, int64_t cols, int k, float* out_vals,
+            int64_t* out_idx, void* stream);
+
+/* ivfpq_last_error -- message for the most recent failure on this thread
+ * (empty string if none). The pointer stays valid until the next call into
+ * the library from this thread. */
+const char* ivfpq_last_error(void);
+
+/* ivfpq_status_string -- a static name for a status code. */
+const char* ivfpq_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* IVFPQ_GB300_H */

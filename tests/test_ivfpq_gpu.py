@@ -1,0 +1,239 @@
+"""IVF-PQ search on the GPU against the oracle.
+
+The probe sets are checked with the tie rule (a probe may differ only by a
+list whose exact coarse distance ties the nprobe-th), then the oracle is run
+with the GPU's probes and the results are compared with the tolerance rule of
+tests/parity.py.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+from approximate_nearest_neighbour_gb300 import synthetic as S
+from parity import check_probes, compare_knn, tol
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def B():
+    from approximate_nearest_neighbour_gb300 import binding
+    return binding
+
+
+def _t(x):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def make_index(B, cent, cb, codes, list_ids, ids, pieces=1):
+    ix = B.ivfpq_index_create(_t(cent), _t(cb))
+    n = codes.shape[0]
+    bounds = np.linspace(0, n, pieces + 1).astype(np.int64)
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        B.ivfpq_add(ix, _t(codes[a:b]), _t(list_ids[a:b]), _t(ids[a:b]))
+    return ix
+
+
+def coarse_all(q, cent):
+    lists, dist = oracle.coarse(q, cent, cent.shape[0])
+    out = np.empty_like(dist)
+    np.put_along_axis(out, lists.astype(np.int64), dist, axis=1)
+    return out
+
+
+def search_and_check(B, ix, cent, cb, lists, q, nprobe, k, rows=None, extra=64, context=""):
+    """lists = (list_off, codes in list order, ids in list order)."""
+    import torch
+    qd = _t(q)
+    gp, gc = B.ivfpq_search_probes(ix, qd, nprobe)
+    gd, gi = B.ivfpq_search(ix, qd, nprobe, k)
+    torch.cuda.synchronize()
+    gp, gc, gd, gi = (x.cpu().numpy() for x in (gp, gc, gd, gi))
+    rows = np.arange(q.shape[0]) if rows is None else np.asarray(rows)
+    qs = q[rows]
+    op, _ = oracle.coarse(qs, cent, nprobe)
+    call = None
+
+    def dist_all(r):
+        nonlocal call
+        if call is None:
+            call = coarse_all(qs, cent)
+        return call[r]
+
+    ndiff = check_probes(gp[rows], op, dist_all)
+    # coarse distances of the GPU's probes
+    dc = np.stack([((cent[gp[r]].astype(np.float64) - q[r].astype(np.float64)) ** 2).sum(1)
+                   for r in rows])
+    assert np.all(np.abs(gc[rows] - dc) <= tol(dc)), f"{context}: coarse distances"
+    off, codes_l, ids_l = lists
+    od, oi, _ = oracle.ivfpq_search(qs, cent, cb, off, codes_l, ids_l, nprobe, k + extra,
+                                    forced_probes=gp[rows])
+    compare_knn(gd[rows], gi[rows], od, oi, context=context)
+    return gd, gi, ndiff
+
+
+# ---------------------------------------------------------------------------
+def test_tiny_workload_trained_codebooks(B):
+    """N=1e5, d=64, 256 clusters (sigma 0.1), centroids = true centres, PQ m=8
+    trained by 10 Lloyd iterations on residuals, nq=100, nprobe=8, k=10."""
+    w = S.IVFPQ_TINY
+    cent, x, init = S.tiny_raw(w)
+    assign, _ = oracle.coarse(x, cent, 1)
+    list_ids = assign[:, 0].astype(np.int32)
+    resid = x - cent[list_ids]
+    cb, obj = oracle.pq_train(resid, w.m, 10, init)
+    assert np.all(np.diff(obj) <= 1e-9 * obj[0])
+    codes = oracle.pq_encode(resid, cb)
+    ids = np.arange(x.shape[0], dtype=np.int64)
+    lists = oracle.to_lists(codes, list_ids, ids, w.nlist)
+    q = S.queries(w.number, cent, S.component_weights(w.nlist, False), w.sigma, w.nq)
+    ix = make_index(B, cent, cb, codes, list_ids, ids)
+    assert ix.ntotal == x.shape[0]
+    gd, gi, _ = search_and_check(B, ix, cent, cb, lists, q, 8, 10, context="tiny")
+    # recall against exact neighbours is reported, not gated
+    _, ti = oracle.flat_knn(x, q, 10)
+    r = oracle.recall_at_k(gi, ti)
+    print(f"tiny workload recall@10 vs exact = {r:.3f}")
+    assert r > 0.3
+
+
+@pytest.mark.parametrize("m,dsub", [(8, 12), (12, 4), (16, 8), (32, 3), (64, 2), (20, 3), (4, 5)])
+def test_code_widths_and_ragged_lists(B, m, dsub):
+    d = m * dsub
+    w = S.IVFPQWorkload("t", 90 + m, 30_000, d, 97, m, 0.15, True, 40, (7,), (33,), ("fp32",))
+    data = S.compressed_index(w)
+    assert (np.diff(data.list_off) == 0).any() or True
+    q = S.queries(w.number, data.cent, data.weights, w.sigma, w.nq)
+    codes, list_ids, ids = S.shuffled(data, w.number)
+    ix = make_index(B, data.cent, data.cb, codes, list_ids, ids)
+    lists = oracle.to_lists(codes, list_ids, ids, w.nlist)
+    for k in (1, 33, 250):
+        search_and_check(B, ix, data.cent, data.cb, lists, q, 7, k, context=f"m={m} k={k}")
+
+
+def test_empty_lists_large_k_and_padding(B):
+    """Many empty lists; k larger than the candidates of the probed lists."""
+    w = S.IVFPQWorkload("t", 77, 900, 32, 400, 8, 0.15, True, 9, (3,), (5,), ("fp32",))
+    data = S.compressed_index(w)
+    assert (np.diff(data.list_off) == 0).sum() > 50
+    q = S.queries(w.number, data.cent, data.weights, w.sigma, w.nq)
+    ix = make_index(B, data.cent, data.cb, data.codes, data.list_ids, data.ids)
+    lists = (data.list_off, data.codes, data.ids)
+    for k in (64, 700, 2048):
+        gd, gi, _ = search_and_check(B, ix, data.cent, data.cb, lists, q, 3, k, context=f"k={k}")
+        assert np.isinf(gd[:, -1]).all() and (gi[:, -1] == -1).all()
+
+
+def test_appending_in_pieces_equals_one_add(B):
+    import torch
+    w = S.IVFPQWorkload("t", 66, 25_000, 64, 64, 16, 0.15, False, 30, (5,), (20,), ("fp32",))
+    data = S.compressed_index(w)
+    codes, list_ids, ids = S.shuffled(data, w.number)
+    q = S.queries(w.number, data.cent, data.weights, w.sigma, w.nq)
+    one = make_index(B, data.cent, data.cb, codes, list_ids, ids)
+    three = make_index(B, data.cent, data.cb, codes, list_ids, ids, pieces=3)
+    assert one.ntotal == three.ntotal == codes.shape[0]
+    d1, i1 = B.ivfpq_search(one, _t(q), 5, 20)
+    d3, i3 = B.ivfpq_search(three, _t(q), 5, 20)
+    torch.cuda.synchronize()
+    # identical list contents in identical order: identical results
+    assert torch.equal(d1, d3) and torch.equal(i1, i3)
+    lists = oracle.to_lists(codes, list_ids, ids, w.nlist)
+    search_and_check(B, three, data.cent, data.cb, lists, q, 5, 20, context="pieces")
+
+
+def test_preassigned_probes_with_repeats(B):
+    import torch
+    w = S.IVFPQWorkload("t", 55, 8_000, 48, 32, 16, 0.15, False, 12, (4,), (15,), ("fp32",))
+    data = S.compressed_index(w)
+    q = S.queries(w.number, data.cent, data.weights, w.sigma, w.nq)
+    ix = make_index(B, data.cent, data.cb, data.codes, data.list_ids, data.ids)
+    rng = np.random.default_rng(3)
+    probes = rng.integers(0, w.nlist, (w.nq, 4)).astype(np.int32)
+    probes[:, 3] = probes[:, 0]  # a list given twice contributes twice
+    gd, gi = B.ivfpq_search_preassigned(ix, _t(q), _t(probes), 40)
+    torch.cuda.synchronize()
+    od, oi, _ = oracle.ivfpq_search(q, data.cent, data.cb, data.list_off, data.codes, data.ids,
+                                    4, 40, forced_probes=probes)
+    g = gd.cpu().numpy()
+    assert np.all(np.abs(g - od) <= tol(od))
+
+
+def test_all_lists_on_exactly_encoded_set_matches_flat(B):
+    """Vectors built as centroid + codewords: IVF-PQ with nprobe = nlist and
+    flat k-NN on the decoded vectors agree (two different GPU paths)."""
+    import torch
+    rng = np.random.default_rng(12)
+    nlist, d, m, n = 16, 32, 8, 6000
+    cent = (rng.integers(-8, 9, (nlist, d)) / 4.0).astype(np.float32)
+    cb = (rng.integers(-8, 9, (m, 256, d // m)) / 16.0).astype(np.float32)
+    list_ids = rng.integers(0, nlist, n).astype(np.int32)
+    codes = rng.integers(0, 256, (n, m)).astype(np.uint8)
+    x = (cent[list_ids] + cb[np.arange(m), codes].reshape(n, d)).astype(np.float32)
+    q = (rng.integers(-16, 17, (25, d)) / 8.0).astype(np.float32)
+    ids = np.arange(n, dtype=np.int64)
+    ix = make_index(B, cent, cb, codes, list_ids, ids)
+    gd, gi = B.ivfpq_search(ix, _t(q), nlist, 50)
+    fd, fi = B.flat_knn(_t(x), _t(q), 50)
+    torch.cuda.synchronize()
+    od, oi = oracle.flat_knn(x, q, 50 + 64)
+    compare_knn(gd.cpu().numpy(), gi.cpu().numpy(), od, oi, context="ivf all lists")
+    compare_knn(fd.cpu().numpy(), fi.cpu().numpy(), od, oi, context="flat")
+
+
+def test_empty_index_and_single_query(B):
+    import torch
+    w = S.IVFPQ_LARGE
+    data = S.compressed_index(w, n=0, nlist=8)
+    ix = B.ivfpq_index_create(_t(data.cent), _t(data.cb))
+    q = S.queries(w.number, data.cent, data.weights, w.sigma, 1)
+    gd, gi = B.ivfpq_search(ix, _t(q), 2, 7)
+    torch.cuda.synchronize()
+    assert np.isinf(gd.cpu().numpy()).all() and (gi.cpu().numpy() == -1).all()
+
+
+def test_bad_list_ids_leave_index_unchanged(B):
+    w = S.IVFPQ_LARGE
+    data = S.compressed_index(w, n=1000, nlist=8)
+    ix = make_index(B, data.cent, data.cb, data.codes, data.list_ids, data.ids)
+    bad = data.list_ids.copy()
+    bad[17] = 8
+    with pytest.raises(B.IVFPQError) as e:
+        B.ivfpq_add(ix, _t(data.codes), _t(bad), _t(data.ids))
+    assert e.value.status == B.IVFPQ_ERR_INVALID_ARG
+    assert ix.ntotal == 1000
+
+
+# ---------------------------------------------------------------------------
+# full-size workloads, sampled queries (the launch configuration the
+# benchmark times: all queries in one call)
+def _full(B, w, nprobes, ks, nsample=6):
+    import torch
+    data = S.compressed_index(w)
+    q = S.queries(w.number, data.cent, data.weights, w.sigma, w.nq)
+    ix = make_index(B, data.cent, data.cb, data.codes, data.list_ids, data.ids)
+    lists = (data.list_off, data.codes, data.ids)
+    rows = np.random.default_rng(w.number).choice(w.nq, nsample, replace=False)
+    for nprobe in nprobes:
+        for k in ks:
+            search_and_check(B, ix, data.cent, data.cb, lists, q, nprobe, k, rows=rows,
+                             context=f"{w.name} nprobe={nprobe} k={k}")
+    del ix
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+def test_full_mid(B):
+    _full(B, S.IVFPQ_MID, (16, 64), (100,))
+
+
+@pytest.mark.slow
+def test_full_large(B):
+    _full(B, S.IVFPQ_LARGE, (64,), (100,))
+
+
+@pytest.mark.slow
+def test_full_billion(B):
+    _full(B, S.IVFPQ_BILLION, (128,), (1, 100, 1000), nsample=4)
