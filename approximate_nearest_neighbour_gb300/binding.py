@@ -41,7 +41,8 @@ SIGNATURES = {
     "ivfpq_search_probes": (_I, [_VP, _VP, _I64, _I, _VP, _VP, _VP]),
     "ivfpq_search_preassigned": (_I, [_VP, _VP, _I64, _I, _VP, _I, _VP, _VP, _VP]),
     "ivfpq_set_profiling": (_I, [_VP, _I]),
-    "ivfpq_stage_times": (_I, [_VP, C.POINTER(C.c_float)]),
+    "ivfpq_stage_times": (_I, [_VP, C.POINTER(C.c_float), C.POINTER(C.c_int)]),
+    "ivfpq_kernel_launches": (C.c_uint64, []),
     "flat_knn": (_I, [_VP, _I64, _I, _VP, _I64, _I, _VP, _VP, _VP]),
     "kselect": (_I, [_VP, _I64, _I64, _I, _VP, _VP, _VP]),
     "ivfpq_last_error": (C.c_char_p, []),
@@ -228,10 +229,17 @@ def ivfpq_set_profiling(index, enable=True):
 
 
 def ivfpq_stage_times(index):
-    """[coarse, plan, scan, merge] milliseconds of the last search."""
+    """([coarse, plan, scan, merge] milliseconds summed over the searches
+    recorded since profiling was enabled, number of searches)."""
     buf = (C.c_float * 4)()
-    _check("ivfpq_stage_times", lib().ivfpq_stage_times(index.handle, buf))
-    return list(buf)
+    n = C.c_int(0)
+    _check("ivfpq_stage_times", lib().ivfpq_stage_times(index.handle, buf, C.byref(n)))
+    return list(buf), n.value
+
+
+def kernel_launches():
+    """Kernels launched by the library since it was loaded."""
+    return int(lib().ivfpq_kernel_launches())
 
 
 def flat_knn(db, queries, k, out_dist=None, out_ids=None, stream=None):

@@ -1,4 +1,5 @@
 // Thread-local error messages and status names of the C ABI.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 
@@ -17,9 +18,14 @@ void set_error(const char* fmt, ...) {
 
 void clear_error() { g_err[0] = 0; }
 
+static std::atomic<unsigned long long> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
 }  // namespace ivfpq
 
 extern "C" const char* ivfpq_last_error(void) { return ivfpq::g_err; }
+
+extern "C" uint64_t ivfpq_kernel_launches(void) { return ivfpq::g_launches.load(); }
 
 extern "C" const char* ivfpq_status_string(int status) {
   switch (status) {

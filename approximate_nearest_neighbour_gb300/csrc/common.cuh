@@ -41,8 +41,33 @@ void clear_error();
     if (s_ != IVFPQ_OK) return s_;   \
   } while (0)
 
-// Checks the launch that was just enqueued.
-#define IVFPQ_LAUNCHED() IVFPQ_CUDA(cudaGetLastError())
+// Number of kernels this library has launched (all threads, all devices).
+void count_launch();
+
+// Checks (and counts) the launch that was just enqueued.
+#define IVFPQ_LAUNCHED()             \
+  do {                               \
+    ::ivfpq::count_launch();         \
+    IVFPQ_CUDA(cudaGetLastError());  \
+  } while (0)
+
+// Same, and on failure reports the kernel's resource attributes.
+#define IVFPQ_LAUNCHED_K(kern, smem, threads)                                                  \
+  do {                                                                                         \
+    ::ivfpq::count_launch();                                                                   \
+    cudaError_t e_ = cudaGetLastError();                                                       \
+    if (e_ != cudaSuccess) {                                                                   \
+      cudaFuncAttributes a_{};                                                                 \
+      cudaFuncGetAttributes(&a_, (const void*)(kern));                                         \
+      cudaGetLastError();                                                                      \
+      ::ivfpq::set_error("launch failed: %s (%s:%d; threads=%d smem=%zu; kernel regs=%d "      \
+                         "max_threads=%d max_dyn_smem=%d static_smem=%zu local=%zu)",          \
+                         cudaGetErrorString(e_), __FILE__, __LINE__, int(threads),            \
+                         size_t(smem), a_.numRegs, a_.maxThreadsPerBlock,                      \
+                         a_.maxDynamicSharedSizeBytes, a_.sharedSizeBytes, a_.localSizeBytes); \
+      return IVFPQ_ERR_CUDA;                                                                   \
+    }                                                                                          \
+  } while (0)
 
 // ---- stream-ordered workspace --------------------------------------------------
 // Frees its allocations on the stream (stream-ordered) when it goes out of
@@ -80,6 +105,20 @@ class Workspace {
   void* p_[kMax];
   int n_ = 0;
 };
+
+// Raises a kernel's dynamic shared-memory limit to `bytes`. The kernel's
+// attributes are read first: that loads its module (kernels are loaded lazily
+// on first use), and an attribute set before the module is loaded was seen
+// to be ignored by the first launch.
+template <class Kern>
+int set_dynamic_smem(Kern kern, size_t bytes) {
+  cudaFuncAttributes a{};
+  IVFPQ_CUDA(cudaFuncGetAttributes(&a, reinterpret_cast<const void*>(kern)));
+  if (size_t(a.maxDynamicSharedSizeBytes) < bytes)
+    IVFPQ_CUDA(cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, int(bytes)));
+  return IVFPQ_OK;
+}
 
 inline int num_sms() {
   static int n = 0;

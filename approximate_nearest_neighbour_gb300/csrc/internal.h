@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <vector>
 
 #include "common.cuh"
@@ -74,8 +75,13 @@ struct ivfpq_index {
   int64_t* ids = nullptr;             // [nblocks * 32], -1 on padding slots
   std::vector<int64_t> h_list_len;    // host mirror of list_len
   int64_t max_list_len = 0;
-  // optional per-stage timing
+  // optional per-stage timing: one set of 5 events per profiled search
+  struct EventSet {
+    cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+    bool recorded[5] = {false, false, false, false, false};
+  };
   bool profile = false;
-  cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
-  bool ev_recorded[5] = {false, false, false, false, false};
+  std::vector<EventSet> ev_sets;
+  size_t ev_used = 0;
+  int cur_set = -1;
 };

@@ -207,8 +207,9 @@ extern "C" int ivfpq_index_destroy(ivfpq_index* ix) {
   cudaFree(ix->list_block_off);
   cudaFree(ix->codes);
   cudaFree(ix->ids);
-  for (auto& e : ix->ev)
-    if (e) cudaEventDestroy(e);
+  for (auto& set : ix->ev_sets)
+    for (auto& e : set.ev)
+      if (e) cudaEventDestroy(e);
   delete ix;
   return IVFPQ_OK;
 }

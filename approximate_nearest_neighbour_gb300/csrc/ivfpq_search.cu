@@ -67,12 +67,25 @@ int launch_scan(const ScanParams& p, int64_t nq, cudaStream_t s) {
   return IVFPQ_ERR_INVALID_ARG;
 }
 
+const size_t kMaxEventSets = 4096;
+
+// Starts a new event set for this search (profiling only).
+void begin_profile(const ivfpq_index* ix) {
+  auto* mix = const_cast<ivfpq_index*>(ix);
+  mix->cur_set = -1;
+  if (!mix->profile || mix->ev_used >= kMaxEventSets) return;
+  if (mix->ev_sets.size() <= mix->ev_used) mix->ev_sets.resize(mix->ev_used + 1);
+  auto& set = mix->ev_sets[mix->ev_used];
+  for (bool& r : set.recorded) r = false;
+  mix->cur_set = int(mix->ev_used++);
+}
+
 void record(const ivfpq_index* ix, int i, cudaStream_t s) {
   auto* mix = const_cast<ivfpq_index*>(ix);
-  if (!mix->profile) return;
-  if (!mix->ev[i]) cudaEventCreate(&mix->ev[i]);
-  cudaEventRecord(mix->ev[i], s);
-  mix->ev_recorded[i] = true;
+  if (mix->cur_set < 0) return;
+  auto& set = mix->ev_sets[mix->cur_set];
+  if (!set.ev[i] && cudaEventCreate(&set.ev[i]) != cudaSuccess) return;
+  if (cudaEventRecord(set.ev[i], s) == cudaSuccess) set.recorded[i] = true;
 }
 
 int coarse_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int nprobe,
@@ -144,10 +157,7 @@ int check_common(const ivfpq_index* ix, const float* queries, int64_t nq, int np
   return IVFPQ_OK;
 }
 
-void reset_events(const ivfpq_index* ix) {
-  auto* mix = const_cast<ivfpq_index*>(ix);
-  for (bool& r : mix->ev_recorded) r = false;
-}
+void reset_events(const ivfpq_index* ix) { begin_profile(ix); }
 
 }  // namespace
 }  // namespace ivfpq
@@ -208,22 +218,26 @@ extern "C" int ivfpq_set_profiling(ivfpq_index* ix, int enable) {
   clear_error();
   IVFPQ_REQUIRE(ix, "ivfpq_set_profiling: null index");
   ix->profile = enable != 0;
+  ix->ev_used = 0;
+  ix->cur_set = -1;
   return IVFPQ_OK;
 }
 
-extern "C" int ivfpq_stage_times(const ivfpq_index* ix, float* ms) {
+extern "C" int ivfpq_stage_times(const ivfpq_index* ix, float* ms, int* nsearches) {
   clear_error();
   IVFPQ_REQUIRE(ix && ms, "ivfpq_stage_times: null pointer");
   for (int i = 0; i < 4; ++i) ms[i] = 0.f;
+  if (nsearches) *nsearches = int(ix->ev_used);
   // stage i spans events (i, i+1); the planning stage has no events of its own
-  const int pairs[4][2] = {{0, 1}, {1, 2}, {2, 3}, {3, 4}};
-  for (int i = 0; i < 4; ++i) {
-    const int a = pairs[i][0], b = pairs[i][1];
-    if (!ix->ev_recorded[a] || !ix->ev_recorded[b]) continue;
-    IVFPQ_CUDA(cudaEventSynchronize(ix->ev[b]));
-    float t = 0.f;
-    IVFPQ_CUDA(cudaEventElapsedTime(&t, ix->ev[a], ix->ev[b]));
-    ms[i] = t;
+  for (size_t k = 0; k < ix->ev_used; ++k) {
+    const auto& set = ix->ev_sets[k];
+    for (int i = 0; i < 4; ++i) {
+      if (!set.recorded[i] || !set.recorded[i + 1]) continue;
+      IVFPQ_CUDA(cudaEventSynchronize(set.ev[i + 1]));
+      float t = 0.f;
+      IVFPQ_CUDA(cudaEventElapsedTime(&t, set.ev[i], set.ev[i + 1]));
+      ms[i] += t;
+    }
   }
   return IVFPQ_OK;
 }

@@ -238,10 +238,10 @@ template <int MW, int K>
 int launch_scan_mw(const ScanParams& p, int64_t nq, cudaStream_t s) {
   auto kern = ivfpq_scan_kernel<MW, K>;
   const size_t smem = scan_smem_bytes(p.m, p.d, K);
-  IVFPQ_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)));
+  IVFPQ_TRY(set_dynamic_smem(kern, smem));
   const int64_t blocks = nq * p.nchunks;
   kern<<<unsigned(blocks), kScanWarps * 32, smem, s>>>(p);
-  IVFPQ_LAUNCHED();
+  IVFPQ_LAUNCHED_K(kern, smem, kScanWarps * 32);
   return IVFPQ_OK;
 }
 

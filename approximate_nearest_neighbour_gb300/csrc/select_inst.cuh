@@ -132,11 +132,7 @@ select_pairs_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restric
 
 template <class Kern>
 static int prepare_smem(Kern kern, size_t bytes) {
-  if (bytes > 48 * 1024) {
-    IVFPQ_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    int(bytes)));
-  }
-  return IVFPQ_OK;
+  return bytes > 48 * 1024 ? set_dynamic_smem(kern, bytes) : IVFPQ_OK;
 }
 
 template <int K, int NW>
@@ -147,7 +143,7 @@ int launch_rows(const float* vals, int64_t rows, int64_t cols, int64_t chunks,
   IVFPQ_TRY(prepare_smem(kern, smem));
   dim3 grid{unsigned(rows), unsigned(chunks), 1u};
   kern<<<grid, NW * 32, smem, s>>>(vals, cols, chunk_len, w);
-  IVFPQ_LAUNCHED();
+  IVFPQ_LAUNCHED_K(kern, smem, NW * 32);
   return IVFPQ_OK;
 }
 
@@ -160,7 +156,7 @@ int launch_pairs(const uint32_t* keys, const uint32_t* idx, int64_t rows, int64_
   IVFPQ_TRY(prepare_smem(kern, smem));
   dim3 grid{unsigned(rows), unsigned(chunks), 1u};
   kern<<<grid, NW * 32, smem, s>>>(keys, idx, len, chunk_len, w);
-  IVFPQ_LAUNCHED();
+  IVFPQ_LAUNCHED_K(kern, smem, NW * 32);
   return IVFPQ_OK;
 }
 

@@ -1,0 +1,353 @@
+"""Benchmark: batched IVF-PQ search on one GB300 (queries/s), with the list
+scan's roofline, the clocks seen during the timed region, an end-to-end figure
+through the C ABI with host buffers, and the CPU oracle as a reported baseline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload (default): N = 2e8 vectors, d = 96, nlist = 65,536, PQ m = 32 x 8 bit
+(6.4 GB of codes resident in HBM), nq = 10,000 queries per step, nprobe = 64,
+k = 100, fp32 lookup tables; seeded synthetic Gaussian mixture (see
+approximate_nearest_neighbour_gb300/synthetic.py). A step is one ivfpq_search
+call over the whole query batch: coarse quantizer, table build + list scan +
+per-chunk selection, and the cross-chunk merge.
+
+With N > 1 (torchrun, one rank per GPU) every rank holds a replica of the index
+and searches its own batch of nq queries (queries are independent, so there is
+no data-path collective; weak scaling). `value` counts the queries of all
+ranks over the slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from approximate_nearest_neighbour_gb300 import synthetic as S  # noqa: E402
+
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_FILE = os.path.join(ROOT, "profiles", "ivfpq_scan_large.md")
+SCAN_SOURCES = ["scan.cuh", "select.cuh", "layout.cuh", "common.cuh"]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--lut", default="fp32", choices=["fp32", "fp16", "fp8"])
+    p.add_argument("--n", type=int, default=None, help="database size override (development)")
+    p.add_argument("--nq", type=int, default=None)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+WORKLOAD = S.IVFPQ_LARGE
+NPROBE, K = 64, 100
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def scan_source_hash():
+    h = hashlib.sha256()
+    for name in SCAN_SOURCES:
+        with open(os.path.join(ROOT, "approximate_nearest_neighbour_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per scan launch from the committed ncu summary, if it was
+    taken on the current scan source; else None."""
+    if not os.path.exists(PROFILE_FILE):
+        return None
+    vals = {}
+    with open(PROFILE_FILE) as f:
+        for line in f:
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("scan_source_sha256") != scan_source_hash():
+        return None
+    try:
+        return float(vals["dram_bytes_per_full_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def make_workload(n=None, nq=None, rank=0):
+    w = WORKLOAD
+    data = S.compressed_index(w, n=n)
+    q = S.queries(w.number, data.cent, data.weights, w.sigma, nq or w.nq, salt=rank)
+    return data, q
+
+
+def cpu_baseline(data, q, lut, target_s=12.0, max_queries=4096):
+    """The oracle, as it stands, on this host's cores, on a bounded sample of
+    the step's queries."""
+    import oracle
+    threads = oracle.NTHREADS
+    lut_type = {"fp32": 0, "fp16": 1, "fp8": 2}[lut]
+    probe = min(2 * threads, q.shape[0])
+    t0 = time.perf_counter()
+    oracle.ivfpq_search(q[:probe], data.cent, data.cb, data.list_off, data.codes, data.ids,
+                        NPROBE, K, lut_type)
+    dt = time.perf_counter() - t0
+    n = int(min(max_queries, q.shape[0], max(probe, target_s / max(dt, 1e-6) * probe)))
+    t0 = time.perf_counter()
+    oracle.ivfpq_search(q[:n], data.cent, data.cb, data.list_off, data.codes, data.ids,
+                        NPROBE, K, lut_type)
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": "queries/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {n} of the {q.shape[0]} step queries, full index, "
+                      f"{threads} threads, {dt:.1f} s"}
+
+
+def emit(obj):
+    print(json.dumps(obj), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    data, q = make_workload(args.n, args.nq)
+    threads = oracle.NTHREADS
+    per_step = max(1, min(q.shape[0], 4 * threads))
+    lut_type = {"fp32": 0, "fp16": 1, "fp8": 2}[args.lut]
+    times = []
+    for i in range(args.warmup + args.steps):
+        sl = slice((i * per_step) % q.shape[0], (i * per_step) % q.shape[0] + per_step)
+        t0 = time.perf_counter()
+        oracle.ivfpq_search(q[sl], data.cent, data.cb, data.list_off, data.codes, data.ids,
+                            NPROBE, K, lut_type)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = per_step * args.steps / total
+    emit({"impl": "reference", "metric": f"IVF-PQ queries/s (k={K}, nprobe={NPROBE})",
+          "value": value, "unit": "queries/s", "n_gpus": args.gpus, "steps": args.steps,
+          "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+          "data": "synthetic", "config": config_dict(args, data),
+          "cpu_baseline": {"value": value, "unit": "queries/s", "cores": threads,
+                           "kind": "oracle",
+                           "sample": f"{per_step} queries per step (of {q.shape[0]}), full index"},
+          "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0,
+                  "d2h_bytes_per_step": 0}})
+
+
+def config_dict(args, data):
+    w = WORKLOAD
+    n = data.codes.shape[0]
+    return {"workload": w.name if args.n is None else f"{w.name}(N={n})", "n": n, "d": w.d,
+            "nlist": w.nlist, "m": w.m, "nq_per_gpu": args.nq or w.nq, "nprobe": NPROBE, "k": K,
+            "lut": args.lut, "parallelism": f"replicas x{args.gpus}",
+            "l2": f"inputs larger than L2 ({n * w.m / 1e9:.1f} GB of PQ codes)"}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from approximate_nearest_neighbour_gb300 import binding as B
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    data, q = make_workload(args.n, args.nq, rank)
+    nq = q.shape[0]
+
+    ix = B.ivfpq_index_create(torch.from_numpy(data.cent).to(dev), torch.from_numpy(data.cb).to(dev))
+    B.ivfpq_add(ix, torch.from_numpy(data.codes).to(dev), torch.from_numpy(data.list_ids).to(dev),
+                torch.from_numpy(data.ids).to(dev))
+    B.ivfpq_set_lut_type(ix, args.lut)
+    qd = torch.from_numpy(q).to(dev)
+    out_d = torch.empty((nq, K), dtype=torch.float32, device=dev)
+    out_i = torch.empty((nq, K), dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # algorithmic bytes of one scan launch: the codes of every probed list
+    probes, _ = B.ivfpq_search_probes(ix, qd, NPROBE, with_dist=False)
+    lens = np.diff(data.list_off)
+    scan_bytes = float(lens[probes.cpu().numpy()].sum()) * WORKLOAD.m
+    scanned_codes = scan_bytes / WORKLOAD.m
+
+    for _ in range(args.warmup):
+        B.ivfpq_search(ix, qd, NPROBE, K, out_d, out_i)
+    torch.cuda.synchronize()
+
+    clocks = Clocks(local)
+    B.ivfpq_set_profiling(ix, True)
+    launches0 = B.kernel_launches()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        B.ivfpq_search(ix, qd, NPROBE, K, out_d, out_i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    launches = B.kernel_launches() - launches0
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    sums, count = B.ivfpq_stage_times(ix)
+    B.ivfpq_set_profiling(ix, False)
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+
+    # end to end through the C ABI: pinned host queries in, host results out
+    qh = torch.from_numpy(q).pin_memory()
+    hd = torch.empty((nq, K), dtype=torch.float32).pin_memory()
+    hi = torch.empty((nq, K), dtype=torch.int64).pin_memory()
+    qbuf = torch.empty_like(qd)
+    for _ in range(2):
+        qbuf.copy_(qh, non_blocking=True)
+        B.ivfpq_search(ix, qbuf, NPROBE, K, out_d, out_i)
+        hd.copy_(out_d, non_blocking=True)
+        hi.copy_(out_i, non_blocking=True)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        qbuf.copy_(qh, non_blocking=True)
+        B.ivfpq_search(ix, qbuf, NPROBE, K, out_d, out_i)
+        hd.copy_(out_d, non_blocking=True)
+        hi.copy_(out_i, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_elapsed = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        t = torch.tensor([e2e_elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_elapsed = float(t.item())
+
+    if rank == 0:
+        peak, peak_kind = peaks()
+        scan_ms = sums[2] / max(count, 1)
+        achieved = scan_bytes / (scan_ms / 1e3) / 1e9
+        traffic = profiled_traffic()
+        if traffic is not None and args.n is not None:
+            traffic = None
+        total_q = nq * world * args.steps
+        line = {
+            "metric": f"IVF-PQ queries/s (k={K}, nprobe={NPROBE})",
+            "value": total_q / elapsed, "unit": "queries/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": config_dict(args, data),
+            "roofline": {"bound": "hbm", "kernel": "ivfpq_scan_kernel", "achieved": achieved,
+                         "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_source": f"{peak_kind} hbm_gbs (copy)",
+                         "traffic": traffic, "algorithmic_bytes_per_launch": scan_bytes,
+                         "launch_ms": scan_ms},
+            "stage_ms": {"coarse": sums[0] / max(count, 1), "scan": scan_ms,
+                         "merge": sums[3] / max(count, 1)},
+            "scanned_codes_per_s": scanned_codes / (scan_ms / 1e3) * world,
+            "e2e": {"value": total_q / e2e_elapsed, "unit": "queries/s",
+                    "h2d_bytes_per_step": int(q.nbytes),
+                    "d2h_bytes_per_step": int(hd.numel() * 4 + hi.numel() * 8)},
+            "gpu_launches": launches,
+            "clocks": clk,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(data, q, args.lut)
+        emit(line)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -122,12 +122,12 @@ int64_t ivfpq_ntotal(const ivfpq_index* index);
  * Source: IVFPQ search steps 1-5 and Eq. (1) ("Custom 8-bit floating point
  * ..." page); lookup tables T_1..T_b and their use in the list scan, two-pass
  * k-selection ("Billion-scale similarity search with GPUs", section 5).
- * For each query: the nprobe nearest centroids (ties to the lower list id),
- * per probed list the table T_j[e] = ||r^(j) - codeword_j(e)||^2 of the
+ * For each query: the nprobe nearest centroids (the order of equal
+ * distances is unspecified), per probed list the table T_j[e] = ||r^(j) - codeword_j(e)||^2 of the
  * residual r = query - centroid, the distance sum_j T_j[code_j] of every
  * stored vector, and the k smallest over all probed lists.
  *  queries   device fp32 [nq, d]
- *  nprobe    1 .. nlist;  k  1 .. IVFPQ_MAX_K
+ *  nprobe    1 .. min(nlist, IVFPQ_MAX_K);  k  1 .. IVFPQ_MAX_K
  *  out_dist  device fp32 [nq, k];  out_ids  device int64 [nq, k]
  * Errors: INVALID_ARG, OOM, CUDA.
  */
@@ -136,7 +136,7 @@ int ivfpq_search(const ivfpq_index* index, const float* queries, int64_t nq, int
 
 /*
  * ivfpq_search_probes -- the coarse-quantizer stage alone: for each query the
- * nprobe nearest list ids (ascending distance, ties to the lower id) and their
+ * nprobe nearest list ids (ascending distance) and their
  * squared distances. Same source and argument rules as ivfpq_search.
  *  out_probes  device int32 [nq, nprobe];  out_coarse  device fp32 [nq, nprobe]
  *  (out_coarse may be NULL)
@@ -156,16 +156,23 @@ int ivfpq_search_preassigned(const ivfpq_index* index, const float* queries, int
                              int64_t* out_ids, void* stream);
 
 /*
- * ivfpq_set_profiling / ivfpq_stage_times -- optional per-stage timing. When
- * enabled, the search entry points record CUDA events on `stream` around each
- * stage; after the stream has completed, ivfpq_stage_times writes the elapsed
- * milliseconds of the most recent search into ms[0..3]:
- * [0] coarse quantizer (distances + top-nprobe), [1] grouping / planning,
- * [2] lookup tables + list scan + per-chunk selection, [3] cross-list merge.
- * Stages that did not run report 0. Synchronizes on the last recorded event.
+ * ivfpq_set_profiling / ivfpq_stage_times -- optional per-stage timing (not
+ * part of the method; a measurement aid). Enabling (or disabling) clears the
+ * history. While enabled, each search entry point records CUDA events on its
+ * `stream` around its stages (up to 4096 searches are kept).
+ * ivfpq_stage_times waits for the recorded events and writes, summed over
+ * the recorded searches, the milliseconds of [0] coarse quantizer (distances
+ * + top-nprobe), [1] grouping / planning, [2] lookup tables + list scan +
+ * per-chunk selection, [3] cross-list merge into ms[0..3], and the number of
+ * recorded searches into *nsearches (may be NULL). Stages that did not run
+ * contribute 0.
  */
 int ivfpq_set_profiling(ivfpq_index* index, int enable);
-int ivfpq_stage_times(const ivfpq_index* index, float* ms);
+int ivfpq_stage_times(const ivfpq_index* index, float* ms, int* nsearches);
+
+/* ivfpq_kernel_launches -- number of CUDA kernels this library has launched
+ * since it was loaded (all threads); a measurement aid. */
+uint64_t ivfpq_kernel_launches(void);
 
 /*
  * flat_knn -- exact brute-force k-NN under squared L2.
