@@ -60,12 +60,12 @@ int knn_by_tiles(const float* Q, int64_t nq, const float* X, int64_t n, int d, i
 
 // ---- the index -------------------------------------------------------------------------
 struct ivfpq_index {
-  int d = 0, nlist = 0, m = 0, nbits = 8, dsub = 0;
+  int d = 0, nlist = 0, m = 0, nbits = 8, dsub = 0, dsub4 = 0;
   int lut_type = IVFPQ_LUT_FP32;
   int device = 0;
   float* centroids = nullptr;   // [nlist, d]
   float* cent_norms = nullptr;  // [nlist]
-  float* codebooks = nullptr;   // [m, 256, dsub]
+  float* codebooks = nullptr;   // [256, m, dsub4], zero-padded to dsub4 = roundup(dsub, 4)
   // inverted lists, interleaved in blocks of 32 vectors
   int64_t ntotal = 0;
   int64_t nblocks = 0;

@@ -43,17 +43,19 @@ __global__ void cent_norms_kernel(const float* __restrict__ c, int64_t nlist, in
   if (threadIdx.x == 0) out[l] = s;
 }
 
-// [m][256][dsub] (input) -> [256][m][dsub] (internal): reading the tables of
-// one reproduction value for consecutive sub-quantizers is then contiguous.
+// [m][256][dsub] (input) -> [256][m][dsub4] (internal), dsub4 = dsub rounded
+// up to a multiple of 4 with zero padding: reading the codewords of one
+// reproduction value for consecutive sub-quantizers is then contiguous and
+// can use 128-bit loads.
 __global__ void transpose_codebooks_kernel(const float* __restrict__ in, int m, int dsub,
-                                           float* __restrict__ out) {
-  const int64_t n = int64_t(m) * 256 * dsub;
+                                           int dsub4, float* __restrict__ out) {
+  const int64_t n = int64_t(m) * 256 * dsub4;
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += int64_t(gridDim.x) * blockDim.x) {
-    const int t = int(i % dsub);
-    const int64_t je = i / dsub;
-    const int e = int(je % 256), j = int(je / 256);
-    out[(int64_t(e) * m + j) * dsub + t] = in[i];
+    const int t = int(i % dsub4);
+    const int64_t ej = i / dsub4;
+    const int j = int(ej % m), e = int(ej / m);
+    out[i] = t < dsub ? in[(int64_t(j) * 256 + e) * dsub + t] : 0.f;
   }
 }
 
@@ -62,10 +64,13 @@ __global__ void histogram_kernel(const int32_t* __restrict__ list_ids, int64_t n
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += int64_t(gridDim.x) * blockDim.x) {
     const int32_t l = list_ids[i];
-    if (l < 0 || l >= nlist)
+    if (l < 0 || l >= nlist) {
       atomicOr(bad, 1);
-    else
-      atomicAdd(counts + l, 1);
+    } else {
+      // one atomic per distinct list among the active lanes of the warp
+      const unsigned peers = __match_any_sync(__activemask(), l);
+      if ((__ffs(peers) - 1) == int(threadIdx.x & 31)) atomicAdd(counts + l, __popc(peers));
+    }
   }
 }
 
@@ -160,7 +165,9 @@ extern "C" int ivfpq_index_create(int d, int nlist, int m, int nbits, const floa
     ivfpq_index_destroy(ix);
     return st;
   };
+  ix->dsub4 = (ix->dsub + 3) & ~3;
   const size_t cb_n = size_t(m) * 256 * ix->dsub;
+  const size_t cb4_n = size_t(m) * 256 * ix->dsub4;
   float* cb_tmp = nullptr;
 #define CREATE_CUDA(expr)                                                            \
   do {                                                                               \
@@ -173,7 +180,7 @@ extern "C" int ivfpq_index_create(int d, int nlist, int m, int nbits, const floa
   } while (0)
   CREATE_CUDA(cudaMalloc(&ix->centroids, size_t(nlist) * d * sizeof(float)));
   CREATE_CUDA(cudaMalloc(&ix->cent_norms, size_t(nlist) * sizeof(float)));
-  CREATE_CUDA(cudaMalloc(&ix->codebooks, cb_n * sizeof(float)));
+  CREATE_CUDA(cudaMalloc(&ix->codebooks, cb4_n * sizeof(float)));
   CREATE_CUDA(cudaMalloc(&cb_tmp, cb_n * sizeof(float)));
   CREATE_CUDA(cudaMalloc(&ix->list_len, size_t(nlist) * sizeof(int32_t)));
   CREATE_CUDA(cudaMalloc(&ix->list_block_off, size_t(nlist + 1) * sizeof(int64_t)));
@@ -185,8 +192,8 @@ extern "C" int ivfpq_index_create(int d, int nlist, int m, int nbits, const floa
   cent_norms_kernel<<<unsigned(ceil_div(nlist, 8)), dim3(32, 8), 0, 0>>>(ix->centroids, nlist, d,
                                                                          ix->cent_norms);
   CREATE_CUDA(cudaGetLastError());
-  transpose_codebooks_kernel<<<grid_for(int64_t(cb_n), 256), 256, 0, 0>>>(cb_tmp, m, ix->dsub,
-                                                                           ix->codebooks);
+  transpose_codebooks_kernel<<<grid_for(int64_t(cb4_n), 256), 256, 0, 0>>>(
+      cb_tmp, m, ix->dsub, ix->dsub4, ix->codebooks);
   CREATE_CUDA(cudaGetLastError());
   CREATE_CUDA(cudaStreamSynchronize(0));
   cudaFree(cb_tmp);

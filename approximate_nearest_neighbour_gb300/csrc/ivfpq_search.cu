@@ -123,6 +123,7 @@ int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int npro
   p.d = ix->d;
   p.m = ix->m;
   p.dsub = ix->dsub;
+  p.dsub4 = ix->dsub4;
   p.nlist = ix->nlist;
   p.nprobe = nprobe;
   p.k = k;

@@ -37,23 +37,23 @@ namespace ivfpq {
 struct ScanParams {
   const float* queries;      // [nq, d]
   const float* centroids;    // [nlist, d]
-  const float* codebooks_t;  // [256, m, dsub]
+  const float* codebooks_t;  // [256, m, dsub4], zero-padded
   const int32_t* probes;     // [nq, nprobe]
   const int32_t* list_len;   // [nlist]
   const int64_t* list_block_off;  // [nlist + 1]
   const uint8_t* codes;      // blocks of 32 * m bytes
   uint32_t* pkeys;           // [nq, nchunks, k]
   uint32_t* pidx;
-  int d, m, dsub, nlist, nprobe, per_chunk, nchunks, k;
+  int d, m, dsub, dsub4, nlist, nprobe, per_chunk, nchunks, k;
 };
 
 constexpr int kScanWarps = 8;
 constexpr int kGroupWords = 256 * 64;  // one group of up to 32 tables
 
-inline size_t scan_smem_bytes(int m, int d, int K) {
+inline size_t scan_smem_bytes(int m, int dsub4, int K) {
   const size_t lut = size_t((m + 31) / 32) * kGroupWords * 4;
   const size_t merge = size_t(kScanWarps) * K * 8;
-  return (lut > merge ? lut : merge) + size_t((d + 3) / 4) * 16;
+  return (lut > merge ? lut : merge) + size_t(m) * dsub4 * 4;
 }
 
 __device__ __forceinline__ uint4 ld_code16(const uint8_t* p) {
@@ -64,6 +64,22 @@ __device__ __forceinline__ uint2 ld_code8(const uint8_t* p) {
 }
 __device__ __forceinline__ uint32_t ld_code4(const uint8_t* p) {
   return __ldcs(reinterpret_cast<const unsigned int*>(p));
+}
+
+// Asks the TMA unit to stream [p, p + bytes) from HBM into L2 (no completion
+// to wait for; the later loads of the scan hit L2). p and bytes are multiples
+// of 16.
+__device__ __forceinline__ void prefetch_l2(const uint8_t* p, int64_t bytes) {
+  for (int64_t o = 0; o < bytes; o += 65536) {
+    const uint32_t n = uint32_t(bytes - o < 65536 ? bytes - o : 65536);
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p + o), "r"(n) : "memory");
+  }
+}
+
+__device__ __forceinline__ void prefetch_list(const ScanParams& p, int l, int m) {
+  if (l < 0 || l >= p.nlist) return;
+  const int64_t nb = (int64_t(p.list_len[l]) + 31) >> 5;
+  if (nb > 0) prefetch_l2(p.codes + p.list_block_off[l] * 32 * m, nb * 32 * m);
 }
 
 // Stored code words of slot `lane` in a block (MW = m / 4 words).
@@ -92,14 +108,19 @@ __device__ __forceinline__ void load_codes(const uint8_t* blk, int lane, uint32_
   }
 }
 
-// Sum of the m table entries selected by the stored code words.
+// Sum of the m table entries selected by the stored code words. The byte
+// offset of entry (code byte e, column lane + s) is e*256 + 4*lane + 4*s; one
+// byte permute builds e*256 + 4*lane from the code word and lane4 = 4*lane,
+// and 4*s (plus the group offset) is a constant.
 template <int MW>
-__device__ __forceinline__ float adc_sum(const uint32_t (&w)[MW], const float* lut_lane) {
+__device__ __forceinline__ float adc_sum(const uint32_t (&w)[MW], const char* lut_bytes,
+                                         uint32_t lane4) {
   float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
   for (int s = 0; s < 4 * MW; ++s) {
-    const uint32_t byte = (w[s >> 2] >> (8 * (s & 3))) & 0xffu;
-    const float v = lut_lane[(s >> 5) * kGroupWords + int(byte) * 64 + (s & 31)];
+    const uint32_t off = __byte_perm(w[s >> 2], lane4, 0x5504u | (uint32_t(s & 3) << 4));
+    const float v = *reinterpret_cast<const float*>(
+        lut_bytes + off + ((s >> 5) * kGroupWords + (s & 31)) * 4);
     if (s & 1)
       acc1 += v;
     else
@@ -108,46 +129,112 @@ __device__ __forceinline__ float adc_sum(const uint32_t (&w)[MW], const float* l
   return acc0 + acc1;
 }
 
-// All m tables of residual r (shared memory, d floats) into `lut`.
-__device__ __forceinline__ void build_lut(float* lut, const float* r, const float* cbt, int m,
-                                          int dsub, int warp, int lane) {
-  const int ngroups = (m + 31) >> 5;
-  for (int g = 0; g < ngroups; ++g) {
-    const int gs = group_size(g, m);
-    float* base = lut + g * kGroupWords;
-    if ((gs & (gs - 1)) == 0) {
-      // Each (table, value) pair computed once, then stored to its 64/gs
-      // columns; lane i starts at a different copy so the stores of one
-      // instruction fall into 32 distinct banks.
-      const int reps = 64 / gs;
-      const int jj = lane % gs, qq = lane / gs;
-      const int j = 32 * g + jj;
-      const float* rj = r + j * dsub;
-      for (int it = warp * 32; it < 256 * gs; it += kScanWarps * 32) {
-        const int e = (it + lane) / gs;
-        const float* c = cbt + (int64_t(e) * m + j) * dsub;
-        float T = 0.f;
-        for (int t = 0; t < dsub; ++t) {
-          const float diff = rj[t] - __ldg(c + t);
-          T = fmaf(diff, diff, T);
-        }
-        float* row = base + e * 64 + jj;
-        for (int s = 0; s < reps; ++s) row[gs * ((s + qq) % reps)] = T;
-      }
-    } else {
-      for (int it = warp * 32 + lane; it < kGroupWords; it += kScanWarps * 32) {
-        const int e = it >> 6, col = it & 63;
-        const int j = 32 * g + col % gs;
-        const float* c = cbt + (int64_t(e) * m + j) * dsub;
-        const float* rj = r + j * dsub;
-        float T = 0.f;
-        for (int t = 0; t < dsub; ++t) {
-          const float diff = rj[t] - __ldg(c + t);
-          T = fmaf(diff, diff, T);
-        }
-        base[it] = T;
-      }
+// Residual r = q - c_l into shared memory as [m][dsub4], zero-padded.
+__device__ __forceinline__ void residual(float* res, const ScanParams& p, int64_t q, int l,
+                                         int m, int tid) {
+  const float* x = p.queries + q * p.d;
+  const float* c = p.centroids + int64_t(l) * p.d;
+  for (int i = tid; i < m * p.dsub4; i += kScanWarps * 32) {
+    const int j = i / p.dsub4, t = i - j * p.dsub4;
+    res[i] = t < p.dsub ? x[j * p.dsub + t] - c[j * p.dsub + t] : 0.f;
+  }
+}
+
+// Tables of group g (sub-quantizers [32g, 32g + GS)) when GS is a power of
+// two and dsub4 = 4*NV: lane -> table jj = lane % GS (fixed, so its residual
+// slice stays in registers) and value e = (it + lane) / GS; each entry is
+// computed once and stored to its 64/GS columns, lane i starting at a
+// different copy so the 32 stores of one instruction hit 32 distinct banks.
+template <int GS, int NV>
+__device__ __forceinline__ void build_group(float* base, const float* res, const float* cbt,
+                                            int m, int g, int warp, int lane) {
+  constexpr int REPS = 64 / GS;
+  constexpr int LOG_GS = GS == 32 ? 5 : GS == 16 ? 4 : GS == 8 ? 3 : 2;
+  const int jj = lane & (GS - 1), qq = lane >> LOG_GS;
+  const int j = 32 * g + jj;
+  float4 rr[NV];
+  const float4* r4 = reinterpret_cast<const float4*>(res) + j * NV;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) rr[i] = r4[i];
+  const float4* cb4 = reinterpret_cast<const float4*>(cbt);
+#pragma unroll 2
+  for (int it = warp * 32; it < 256 * GS; it += kScanWarps * 32) {
+    const int e = (it + lane) >> LOG_GS;
+    const float4* c = cb4 + (e * m + j) * NV;
+    float T = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const float4 cv = __ldg(c + i);
+      float df = rr[i].x - cv.x;
+      T = fmaf(df, df, T);
+      df = rr[i].y - cv.y;
+      T = fmaf(df, df, T);
+      df = rr[i].z - cv.z;
+      T = fmaf(df, df, T);
+      df = rr[i].w - cv.w;
+      T = fmaf(df, df, T);
     }
+    float* row = base + e * 64 + jj;
+#pragma unroll
+    for (int s = 0; s < REPS; ++s) row[GS * ((s + qq) & (REPS - 1))] = T;
+  }
+}
+
+// Any group size / dsub4: every (row, column) word is computed directly.
+__device__ __forceinline__ void build_group_generic(float* base, const float* res,
+                                                    const float* cbt, int m, int dsub4, int g,
+                                                    int warp, int lane) {
+  const int gs = group_size(g, m);
+  const int nv = dsub4 >> 2;
+  const float4* cb4 = reinterpret_cast<const float4*>(cbt);
+  const float4* r4 = reinterpret_cast<const float4*>(res);
+  for (int it = warp * 32 + lane; it < kGroupWords; it += kScanWarps * 32) {
+    const int e = it >> 6, col = it & 63;
+    const int j = 32 * g + col % gs;
+    float T = 0.f;
+    for (int i = 0; i < nv; ++i) {
+      const float4 cv = __ldg(cb4 + (e * m + j) * nv + i);
+      const float4 rv = r4[j * nv + i];
+      float df = rv.x - cv.x;
+      T = fmaf(df, df, T);
+      df = rv.y - cv.y;
+      T = fmaf(df, df, T);
+      df = rv.z - cv.z;
+      T = fmaf(df, df, T);
+      df = rv.w - cv.w;
+      T = fmaf(df, df, T);
+    }
+    base[it] = T;
+  }
+}
+
+template <int GS>
+__device__ __forceinline__ void build_group_nv(float* base, const float* res, const float* cbt,
+                                               int m, int dsub4, int g, int warp, int lane) {
+  switch (dsub4 >> 2) {
+    case 1: build_group<GS, 1>(base, res, cbt, m, g, warp, lane); break;
+    case 2: build_group<GS, 2>(base, res, cbt, m, g, warp, lane); break;
+    case 3: build_group<GS, 3>(base, res, cbt, m, g, warp, lane); break;
+    case 4: build_group<GS, 4>(base, res, cbt, m, g, warp, lane); break;
+    default: build_group_generic(base, res, cbt, m, dsub4, g, warp, lane); break;
+  }
+}
+
+// All m tables of the residual into `lut` (MW > 0: m = 4*MW known).
+template <int MW>
+__device__ __forceinline__ void build_lut(float* lut, const float* res, const float* cbt,
+                                          int m, int dsub4, int warp, int lane) {
+  if constexpr (MW > 0) {
+    constexpr int NG = (4 * MW + 31) / 32;
+    constexpr int GS = 4 * MW < 32 ? 4 * MW : 32;
+    static_assert((GS & (GS - 1)) == 0, "power-of-two group");
+#pragma unroll
+    for (int g = 0; g < NG; ++g)
+      build_group_nv<GS>(lut + g * kGroupWords, res, cbt, m, dsub4, g, warp, lane);
+  } else {
+    const int ng = (m + 31) >> 5;
+    for (int g = 0; g < ng; ++g)
+      build_group_generic(lut + g * kGroupWords, res, cbt, m, dsub4, g, warp, lane);
   }
 }
 
@@ -171,16 +258,19 @@ ivfpq_scan_kernel(const ScanParams p) {
   ws.init(lane);
   const int p0 = chunk * p.per_chunk;
   const int p1 = min(p.nprobe, p0 + p.per_chunk);
-  const float* lut_lane = lut + lane;
+  const int32_t* qprobes = p.probes + q * p.nprobe;
+  const char* lut_bytes = reinterpret_cast<const char*>(lut);
+  const uint32_t lane4 = uint32_t(lane) * 4;
+  if (tid == 0 && p0 < p1) prefetch_list(p, qprobes[p0], m);
 
   for (int pi = p0; pi < p1; ++pi) {
-    const int l = p.probes[q * p.nprobe + pi];
+    const int l = qprobes[pi];
+    if (tid == 0 && pi + 1 < p1) prefetch_list(p, qprobes[pi + 1], m);
     if (l < 0 || l >= p.nlist) continue;  // same value for the whole block
     __syncthreads();  // the previous list's scan no longer reads the tables
-    for (int t = tid; t < p.d; t += NW * 32)
-      res[t] = p.queries[q * p.d + t] - p.centroids[int64_t(l) * p.d + t];
+    residual(res, p, q, l, m, tid);
     __syncthreads();
-    build_lut(lut, res, p.codebooks_t, m, p.dsub, warp, lane);
+    build_lut<MW>(lut, res, p.codebooks_t, m, p.dsub4, warp, lane);
     __syncthreads();
     const int len = p.list_len[l];
     const int64_t boff = p.list_block_off[l];
@@ -193,13 +283,14 @@ ivfpq_scan_kernel(const ScanParams p) {
       for (; b < nb; b += NW) {
         const int bn = b + NW;
         if (bn < nb) load_codes<MW>(lcodes + int64_t(bn) * 32 * m, lane, nxt);
-        const float dist = adc_sum<MW>(cur, lut_lane);
+        const float dist = adc_sum<MW>(cur, lut_bytes, lane4);
         const bool valid = b * 32 + lane < len;
         ws.add(valid ? __float_as_uint(dist) : kSentinelKey, uint32_t((boff + b) * 32 + lane));
 #pragma unroll
         for (int w = 0; w < MW; ++w) cur[w] = nxt[w];
       }
     } else {
+      const float* lut_lane = lut + lane;
       for (int b = warp; b < nb; b += NW) {
         const uint8_t* blk = lcodes + int64_t(b) * 32 * m;
         float dist = 0.f;
@@ -237,7 +328,7 @@ ivfpq_scan_kernel(const ScanParams p) {
 template <int MW, int K>
 int launch_scan_mw(const ScanParams& p, int64_t nq, cudaStream_t s) {
   auto kern = ivfpq_scan_kernel<MW, K>;
-  const size_t smem = scan_smem_bytes(p.m, p.d, K);
+  const size_t smem = scan_smem_bytes(p.m, p.dsub4, K);
   IVFPQ_TRY(set_dynamic_smem(kern, smem));
   const int64_t blocks = nq * p.nchunks;
   kern<<<unsigned(blocks), kScanWarps * 32, smem, s>>>(p);

@@ -49,6 +49,7 @@ def parse():
     p.add_argument("--lut", default="fp32", choices=["fp32", "fp16", "fp8"])
     p.add_argument("--n", type=int, default=None, help="database size override (development)")
     p.add_argument("--nq", type=int, default=None)
+    p.add_argument("--nlist", type=int, default=None, help="list count override (development)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
@@ -144,9 +145,9 @@ class Clocks:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def make_workload(n=None, nq=None, rank=0):
+def make_workload(n=None, nq=None, rank=0, nlist=None):
     w = WORKLOAD
-    data = S.compressed_index(w, n=n)
+    data = S.compressed_index(w, n=n, nlist=nlist)
     q = S.queries(w.number, data.cent, data.weights, w.sigma, nq or w.nq, salt=rank)
     return data, q
 
@@ -182,7 +183,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle
-    data, q = make_workload(args.n, args.nq)
+    data, q = make_workload(args.n, args.nq, 0, args.nlist)
     threads = oracle.NTHREADS
     per_step = max(1, min(q.shape[0], 4 * threads))
     lut_type = {"fp32": 0, "fp16": 1, "fp8": 2}[args.lut]
@@ -211,8 +212,10 @@ def run_reference(args):
 def config_dict(args, data):
     w = WORKLOAD
     n = data.codes.shape[0]
-    return {"workload": w.name if args.n is None else f"{w.name}(N={n})", "n": n, "d": w.d,
-            "nlist": w.nlist, "m": w.m, "nq_per_gpu": args.nq or w.nq, "nprobe": NPROBE, "k": K,
+    nlist = data.cent.shape[0]
+    scaled = args.n is not None or args.nlist is not None
+    return {"workload": w.name if not scaled else f"{w.name}(N={n},nlist={nlist})", "n": n,
+            "d": w.d, "nlist": nlist, "m": w.m, "nq_per_gpu": args.nq or w.nq, "nprobe": NPROBE, "k": K,
             "lut": args.lut, "parallelism": f"replicas x{args.gpus}",
             "l2": f"inputs larger than L2 ({n * w.m / 1e9:.1f} GB of PQ codes)"}
 
@@ -227,7 +230,7 @@ def run_ours(args):
         dist.init_process_group("nccl", init_method="env://")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    data, q = make_workload(args.n, args.nq, rank)
+    data, q = make_workload(args.n, args.nq, rank, args.nlist)
     nq = q.shape[0]
 
     ix = B.ivfpq_index_create(torch.from_numpy(data.cent).to(dev), torch.from_numpy(data.cb).to(dev))
@@ -309,7 +312,7 @@ def run_ours(args):
         scan_ms = sums[2] / max(count, 1)
         achieved = scan_bytes / (scan_ms / 1e3) / 1e9
         traffic = profiled_traffic()
-        if traffic is not None and args.n is not None:
+        if traffic is not None and (args.n is not None or args.nlist is not None):
             traffic = None
         total_q = nq * world * args.steps
         line = {
