@@ -45,6 +45,7 @@ SIGNATURES = {
     "ivfpq_kernel_launches": (C.c_uint64, []),
     "flat_knn": (_I, [_VP, _I64, _I, _VP, _I64, _I, _VP, _VP, _VP]),
     "kselect": (_I, [_VP, _I64, _I64, _I, _VP, _VP, _VP]),
+    "kselect_noalloc": (_I, [_VP, _I64, _I64, _I, _VP, _VP, _VP]),
     "ivfpq_last_error": (C.c_char_p, []),
     "ivfpq_status_string": (C.c_char_p, [_I]),
 }
@@ -269,4 +270,19 @@ def kselect(vals, k, out_vals=None, out_idx=None, stream=None):
         out_idx = torch.empty((rows, k), dtype=torch.int64, device=vals.device)
     _check("kselect", lib().kselect(_ptr(vals), rows, cols, k, _ptr(out_vals), _ptr(out_idx),
                                      _stream(stream)))
+    return out_vals, out_idx
+
+
+def kselect_noalloc(vals, k, out_vals, out_idx, stream=None):
+    """kselect through the entry point that allocates no device memory; the
+    caller provides the outputs (fp32 and int64, [rows, k])."""
+    torch = _torch()
+    _need(vals, torch.float32, "vals", 2)
+    _need(out_vals, torch.float32, "out_vals", 2)
+    _need(out_idx, torch.int64, "out_idx", 2)
+    rows, cols = vals.shape
+    if tuple(out_vals.shape) != (rows, k) or tuple(out_idx.shape) != (rows, k):
+        raise ValueError("kselect_noalloc: outputs must be [rows, k]")
+    _check("kselect_noalloc", lib().kselect_noalloc(_ptr(vals), rows, cols, k, _ptr(out_vals),
+                                                     _ptr(out_idx), _stream(stream)))
     return out_vals, out_idx

@@ -200,6 +200,27 @@ int flat_knn(const float* db, int64_t n, int d, const float* queries, int64_t nq
 int kselect(const float* vals, int64_t rows, int64_t cols, int k, float* out_vals,
             int64_t* out_idx, void* stream);
 
+/*
+ * kselect_noalloc -- kselect for callers that cannot allocate device memory
+ * while they run. No passage of the pages corresponds to it; it exists for
+ * callers such as a process whose device memory is fully reserved up front by
+ * another allocator, or a latency-critical loop that may not wait on an
+ * allocator. kselect takes its two-pass workspace from the stream-ordered
+ * pool; this variant allocates nothing: its partial results live in one fixed
+ * 8 MiB device array that every GPU loading the library holds until the
+ * library is unloaded.
+ *  Arguments, layout and results as kselect (the caller passes inputs and
+ *  outputs). Limit: rows * k <= 1,048,576; larger problems return
+ *  IVFPQ_ERR_INVALID_ARG with a message naming the limit.
+ *  The first call on a device sets up the array's device address on that
+ *  device (a runtime symbol lookup); make that first call before any stream
+ *  capture. All calls on one device share that device's array, so calls whose
+ *  work overlaps on the GPU (for example on two streams) race and must be
+ *  ordered by the caller. Nothing left in the array by an earlier call is read.
+ */
+int kselect_noalloc(const float* vals, int64_t rows, int64_t cols, int k, float* out_vals,
+                    int64_t* out_idx, void* stream);
+
 /* ivfpq_last_error -- message for the most recent failure on this thread
  * (empty string if none). The pointer stays valid until the next call into
  * the library from this thread. */
