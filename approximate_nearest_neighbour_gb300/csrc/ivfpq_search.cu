@@ -108,10 +108,6 @@ void plan_chunks(int64_t nq, int nprobe, int* per_chunk, int* nchunks) {
 
 int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int nprobe,
                const int32_t* probes, int k, float* out_dist, int64_t* out_ids, cudaStream_t s) {
-  if (ix->lut_type != IVFPQ_LUT_FP32) {
-    set_error("lookup-table type %d is not available in this build of the scan", ix->lut_type);
-    return IVFPQ_ERR_UNSUPPORTED;
-  }
   ScanParams p;
   p.queries = queries;
   p.centroids = ix->centroids;
@@ -127,6 +123,7 @@ int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int npro
   p.nlist = ix->nlist;
   p.nprobe = nprobe;
   p.k = k;
+  p.lut_type = ix->lut_type;
   plan_chunks(nq, nprobe, &p.per_chunk, &p.nchunks);
   Workspace ws(s);
   const size_t np = size_t(nq) * p.nchunks * k;

@@ -28,6 +28,9 @@
 // (layout.cuh) so that the byte lane i needs at step s is simply stored byte s.
 #pragma once
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 #include "internal.h"
 #include "layout.cuh"
 #include "select.cuh"
@@ -45,6 +48,7 @@ struct ScanParams {
   uint32_t* pkeys;           // [nq, nchunks, k]
   uint32_t* pidx;
   int d, m, dsub, dsub4, nlist, nprobe, per_chunk, nchunks, k;
+  int lut_type;              // IVFPQ_LUT_FP32 / FP16 / FP8
 };
 
 constexpr int kScanWarps = 8;
@@ -108,25 +112,95 @@ __device__ __forceinline__ void load_codes(const uint8_t* blk, int lane, uint32_
   }
 }
 
+// One table entry of the given storage type at a byte address (each entry
+// occupies a 4-byte slot; binary16 and E4M3 values sit in its low bytes).
+template <int LT>
+__device__ __forceinline__ float lut_load(const char* addr) {
+  if constexpr (LT == IVFPQ_LUT_FP32) {
+    return *reinterpret_cast<const float*>(addr);
+  } else if constexpr (LT == IVFPQ_LUT_FP16) {
+    return __half2float(*reinterpret_cast<const __half*>(addr));
+  } else {
+    const __nv_fp8_storage_t b = *reinterpret_cast<const __nv_fp8_storage_t*>(addr);
+    return __half2float(__half(__nv_cvt_fp8_to_halfraw(b, __NV_E4M3)));
+  }
+}
+
 // Sum of the m table entries selected by the stored code words. The byte
 // offset of entry (code byte e, column lane + s) is e*256 + 4*lane + 4*s; one
 // byte permute builds e*256 + 4*lane from the code word and lane4 = 4*lane,
-// and 4*s (plus the group offset) is a constant.
-template <int MW>
+// and 4*s (plus the group offset) is a constant. Sums are in fp32 for every
+// table type (E4M3 sums are scaled by the caller).
+template <int MW, int LT>
 __device__ __forceinline__ float adc_sum(const uint32_t (&w)[MW], const char* lut_bytes,
                                          uint32_t lane4) {
   float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
   for (int s = 0; s < 4 * MW; ++s) {
     const uint32_t off = __byte_perm(w[s >> 2], lane4, 0x5504u | (uint32_t(s & 3) << 4));
-    const float v = *reinterpret_cast<const float*>(
-        lut_bytes + off + ((s >> 5) * kGroupWords + (s & 31)) * 4);
+    const float v =
+        lut_load<LT>(lut_bytes + off + ((s >> 5) * kGroupWords + (s & 31)) * 4);
     if (s & 1)
       acc1 += v;
     else
       acc0 += v;
   }
   return acc0 + acc1;
+}
+
+// Converts the fp32 tables in place to the storage type (all words of the
+// groups; every thread of the block takes part). binary16: round to nearest
+// even. E4M3: one scale per table set, s = max T / 448 (the largest finite
+// E4M3 value), entries stored as E4M3(T / s) with round-to-nearest-even and
+// saturation; *scale receives s. Ends with the block synchronized.
+__device__ __forceinline__ void quantize_lut(uint32_t* lut, int nwords, int lut_type,
+                                             float* scale, uint32_t* red, int tid) {
+  if (lut_type == IVFPQ_LUT_FP16) {
+    for (int i = tid; i < nwords; i += kScanWarps * 32)
+      lut[i] = __half_as_ushort(__float2half_rn(__uint_as_float(lut[i])));
+    __syncthreads();
+    return;
+  }
+  // E4M3: block-wide maximum first (entries are >= 0, so their bits order
+  // like unsigned integers)
+  uint32_t mx = 0;
+  for (int i = tid; i < nwords; i += kScanWarps * 32) mx = max(mx, lut[i]);
+#pragma unroll
+  for (int o = 16; o >= 1; o /= 2) mx = max(mx, __shfl_xor_sync(kFullMask, mx, o));
+  if (tid == 0) *red = 0;
+  __syncthreads();
+  if ((tid & 31) == 0) atomicMax(red, mx);
+  __syncthreads();
+  const float tmax = __uint_as_float(*red);
+  const float s = tmax > 0.f ? tmax / 448.f : 1.f;
+  const float inv = tmax > 0.f ? 448.f / tmax : 1.f;
+  for (int i = tid; i < nwords; i += kScanWarps * 32) {
+    const float v = __uint_as_float(lut[i]) * inv;
+    lut[i] = uint32_t(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+  }
+  if (tid == 0) *scale = s;
+  __syncthreads();
+}
+
+// Scans blocks warp, warp + NW, ... of one list with tables of type LT.
+template <int MW, int LT, class WS>
+__device__ __forceinline__ void scan_list(WS& ws, const uint8_t* lcodes, int64_t boff, int nb,
+                                          int len, int m, const char* lut_bytes,
+                                          uint32_t lane4, float scale, int warp, int lane) {
+  constexpr int NW = kScanWarps;
+  uint32_t cur[MW], nxt[MW];
+  int b = warp;
+  if (b < nb) load_codes<MW>(lcodes + int64_t(b) * 32 * m, lane, cur);
+  for (; b < nb; b += NW) {
+    const int bn = b + NW;
+    if (bn < nb) load_codes<MW>(lcodes + int64_t(bn) * 32 * m, lane, nxt);
+    float dist = adc_sum<MW, LT>(cur, lut_bytes, lane4);
+    if (LT == IVFPQ_LUT_FP8) dist *= scale;
+    const bool valid = b * 32 + lane < len;
+    ws.add(valid ? __float_as_uint(dist) : kSentinelKey, uint32_t((boff + b) * 32 + lane));
+#pragma unroll
+    for (int w = 0; w < MW; ++w) cur[w] = nxt[w];
+  }
 }
 
 // Residual r = q - c_l into shared memory as [m][dsub4], zero-padded.
@@ -238,8 +312,16 @@ __device__ __forceinline__ void build_lut(float* lut, const float* res, const fl
   }
 }
 
+// Blocks per SM that the shared-memory tables allow (64 KB per group of 32
+// sub-quantizers, 64 KB of block-merge area up to K = 1024), given to the
+// compiler so that registers do not become the tighter limit.
 template <int MW, int K>
-__global__ void __launch_bounds__(kScanWarps * 32)
+constexpr int scan_min_blocks() {
+  return (MW > 0 && MW <= 8 && K <= 1024) ? 3 : 1;
+}
+
+template <int MW, int K>
+__global__ void __launch_bounds__(kScanWarps * 32, (scan_min_blocks<MW, K>()))
 ivfpq_scan_kernel(const ScanParams p) {
   constexpr int T = ThreadQ<K>::value;
   constexpr int NW = kScanWarps;
@@ -256,6 +338,8 @@ ivfpq_scan_kernel(const ScanParams p) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   WarpSelect<K, T> ws;
   ws.init(lane);
+  __shared__ float lut_scale;  // E4M3 tables: the scale of the current table set
+  __shared__ uint32_t lut_red;
   const int p0 = chunk * p.per_chunk;
   const int p1 = min(p.nprobe, p0 + p.per_chunk);
   const int32_t* qprobes = p.probes + q * p.nprobe;
@@ -272,25 +356,24 @@ ivfpq_scan_kernel(const ScanParams p) {
     __syncthreads();
     build_lut<MW>(lut, res, p.codebooks_t, m, p.dsub4, warp, lane);
     __syncthreads();
+    if (p.lut_type != IVFPQ_LUT_FP32)
+      quantize_lut(scan_smem, lut_words, p.lut_type, &lut_scale, &lut_red, tid);
     const int len = p.list_len[l];
     const int64_t boff = p.list_block_off[l];
     const int nb = (len + 31) >> 5;
     const uint8_t* lcodes = p.codes + boff * 32 * m;
     if constexpr (MW > 0) {
-      uint32_t cur[MW], nxt[MW];
-      int b = warp;
-      if (b < nb) load_codes<MW>(lcodes + int64_t(b) * 32 * m, lane, cur);
-      for (; b < nb; b += NW) {
-        const int bn = b + NW;
-        if (bn < nb) load_codes<MW>(lcodes + int64_t(bn) * 32 * m, lane, nxt);
-        const float dist = adc_sum<MW>(cur, lut_bytes, lane4);
-        const bool valid = b * 32 + lane < len;
-        ws.add(valid ? __float_as_uint(dist) : kSentinelKey, uint32_t((boff + b) * 32 + lane));
-#pragma unroll
-        for (int w = 0; w < MW; ++w) cur[w] = nxt[w];
-      }
+      if (p.lut_type == IVFPQ_LUT_FP32)
+        scan_list<MW, IVFPQ_LUT_FP32>(ws, lcodes, boff, nb, len, m, lut_bytes, lane4, 1.f, warp,
+                                      lane);
+      else if (p.lut_type == IVFPQ_LUT_FP16)
+        scan_list<MW, IVFPQ_LUT_FP16>(ws, lcodes, boff, nb, len, m, lut_bytes, lane4, 1.f, warp,
+                                      lane);
+      else
+        scan_list<MW, IVFPQ_LUT_FP8>(ws, lcodes, boff, nb, len, m, lut_bytes, lane4, lut_scale,
+                                     warp, lane);
     } else {
-      const float* lut_lane = lut + lane;
+      const char* lut_lane = lut_bytes + lane4;
       for (int b = warp; b < nb; b += NW) {
         const uint8_t* blk = lcodes + int64_t(b) * 32 * m;
         float dist = 0.f;
@@ -301,9 +384,13 @@ ivfpq_scan_kernel(const ScanParams p) {
           for (int bb = 0; bb < 4; ++bb) {
             const int s = s0 + bb;
             const uint32_t byte = (word >> (8 * bb)) & 0xffu;
-            dist += lut_lane[(s >> 5) * kGroupWords + int(byte) * 64 + (s & 31)];
+            const char* a = lut_lane + ((s >> 5) * kGroupWords + int(byte) * 64 + (s & 31)) * 4;
+            dist += p.lut_type == IVFPQ_LUT_FP32   ? lut_load<IVFPQ_LUT_FP32>(a)
+                    : p.lut_type == IVFPQ_LUT_FP16 ? lut_load<IVFPQ_LUT_FP16>(a)
+                                                   : lut_load<IVFPQ_LUT_FP8>(a);
           }
         }
+        if (p.lut_type == IVFPQ_LUT_FP8) dist *= lut_scale;
         const bool valid = b * 32 + lane < len;
         ws.add(valid ? __float_as_uint(dist) : kSentinelKey, uint32_t((boff + b) * 32 + lane));
       }

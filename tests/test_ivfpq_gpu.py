@@ -237,3 +237,53 @@ def test_full_large(B):
 @pytest.mark.slow
 def test_full_billion(B):
     _full(B, S.IVFPQ_BILLION, (128,), (1, 100, 1000), nsample=4)
+
+
+# ---------------------------------------------------------------------------
+# reduced-precision lookup tables
+def _variant_run(B, data, q, nprobe, k, lut):
+    import torch
+    ix = make_index(B, data.cent, data.cb, data.codes, data.list_ids, data.ids)
+    B.ivfpq_set_lut_type(ix, lut)
+    gp, _ = B.ivfpq_search_probes(ix, _t(q), nprobe)
+    gd, gi = B.ivfpq_search(ix, _t(q), nprobe, k)
+    torch.cuda.synchronize()
+    return gp.cpu().numpy(), gd.cpu().numpy(), gi.cpu().numpy()
+
+
+@pytest.mark.parametrize("lut,rtol,min_recall", [("fp16", 2e-3, 0.99), ("fp8", 3e-2, 0.97)])
+@pytest.mark.parametrize("m,dsub", [(32, 3), (8, 12), (16, 4)])
+def test_reduced_tables_follow_the_oracle_variant(B, lut, rtol, min_recall, m, dsub):
+    """The GPU's binary16 / E4M3 tables against the oracle's tables of the
+    same type (encoders written from the formats' definitions): ids agree up
+    to rounding-order ties and distances to within the format's precision."""
+    w = S.IVFPQWorkload("t", 120 + m, 40_000, m * dsub, 50, m, 0.15, False, 24, (6,), (40,),
+                        (lut,))
+    data = S.compressed_index(w)
+    q = S.queries(w.number, data.cent, data.weights, w.sigma, w.nq)
+    gp, gd, gi = _variant_run(B, data, q, 6, 40, lut)
+    lt = {"fp16": oracle.LUT_FP16, "fp8": oracle.LUT_FP8}[lut]
+    od, oi, _ = oracle.ivfpq_search(q, data.cent, data.cb, data.list_off, data.codes, data.ids,
+                                    6, 40, lt, forced_probes=gp)
+    assert oracle.recall_at_k(gi, oi) >= min_recall
+    assert np.all(np.abs(gd - od) <= rtol * np.abs(od) + 1e-5)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("lut,gate", [("fp16", 0.99), ("fp8", 0.95)])
+def test_full_large_reduced_table_recall_gates(B, lut, gate):
+    """Large workload (2e8 vectors, m = 32, nprobe = 64, k = 100): recall@100
+    of the fp16 / E4M3 table variants against the fp32 oracle on a seeded
+    sample of 256 queries (gates: 0.99 and 0.95)."""
+    import torch
+    w = S.IVFPQ_LARGE
+    data = S.compressed_index(w)
+    q = S.queries(w.number, data.cent, data.weights, w.sigma, w.nq)
+    gp, gd, gi = _variant_run(B, data, q, 64, 100, lut)
+    rows = np.random.default_rng(4).choice(w.nq, 256, replace=False)
+    _, oi, _ = oracle.ivfpq_search(q[rows], data.cent, data.cb, data.list_off, data.codes,
+                                   data.ids, 64, 100, forced_probes=gp[rows])
+    r = oracle.recall_at_k(gi[rows], oi)
+    print(f"{lut} recall@100 vs fp32 oracle = {r:.4f}")
+    assert r >= gate
+    torch.cuda.empty_cache()
