@@ -10,7 +10,7 @@
 #include <algorithm>
 
 #include "internal.h"
-#include "scan.cuh"
+#include "scan2.cuh"
 
 namespace ivfpq {
 
@@ -29,6 +29,36 @@ IVFPQ_EXTERN_SCAN(16, 32)
 IVFPQ_EXTERN_SCAN(16, 64)
 IVFPQ_EXTERN_SCAN(16, 128)
 IVFPQ_EXTERN_SCAN(16, 256)
+
+#define IVFPQ_EXTERN_SCAN2(MW, DS)                                                                 \
+  extern template int launch_scan2<MW, DS, 32>(const ScanParams&, int64_t, cudaStream_t);         \
+  extern template int launch_scan2<MW, DS, 64>(const ScanParams&, int64_t, cudaStream_t);         \
+  extern template int launch_scan2<MW, DS, 128>(const ScanParams&, int64_t, cudaStream_t);        \
+  extern template int launch_scan2<MW, DS, 256>(const ScanParams&, int64_t, cudaStream_t);
+IVFPQ_EXTERN_SCAN2(8, 3)
+IVFPQ_EXTERN_SCAN2(8, 4)
+IVFPQ_EXTERN_SCAN2(4, 8)
+IVFPQ_EXTERN_SCAN2(4, 4)
+IVFPQ_EXTERN_SCAN2(2, 12)
+IVFPQ_EXTERN_SCAN2(2, 8)
+
+// The register-codebook kernel (scan2.cuh) for fp32 tables, k <= 256 and the
+// (m, d/m) shapes it is built for; 1 = launched, 0 = not applicable.
+template <int K>
+int try_scan2_k(const ScanParams& p, int64_t nq, cudaStream_t s, int* launched) {
+  *launched = 1;
+  const int key = p.m * 100 + p.dsub;
+  switch (key) {
+    case 3203: return launch_scan2<8, 3, K>(p, nq, s);
+    case 3204: return launch_scan2<8, 4, K>(p, nq, s);
+    case 1608: return launch_scan2<4, 8, K>(p, nq, s);
+    case 1604: return launch_scan2<4, 4, K>(p, nq, s);
+    case 812: return launch_scan2<2, 12, K>(p, nq, s);
+    case 808: return launch_scan2<2, 8, K>(p, nq, s);
+  }
+  *launched = 0;
+  return IVFPQ_OK;
+}
 
 // Code words per vector as a template argument where a specialised kernel
 // exists (m = 8, 16, 32; m = 64 for K <= 256); 0 selects the generic kernel.
@@ -54,6 +84,16 @@ int queue_len(int k) {
 }
 
 int launch_scan(const ScanParams& p, int64_t nq, cudaStream_t s) {
+  if (p.lut_type == IVFPQ_LUT_FP32 && p.m * p.dsub == p.d) {
+    int launched = 0, st = IVFPQ_OK;
+    switch (queue_len(p.k)) {
+      case 32: st = try_scan2_k<32>(p, nq, s, &launched); break;
+      case 64: st = try_scan2_k<64>(p, nq, s, &launched); break;
+      case 128: st = try_scan2_k<128>(p, nq, s, &launched); break;
+      case 256: st = try_scan2_k<256>(p, nq, s, &launched); break;
+    }
+    if (launched || st != IVFPQ_OK) return st;
+  }
   switch (queue_len(p.k)) {
     case 32: return launch_scan_k<32>(p, nq, s);
     case 64: return launch_scan_k<64>(p, nq, s);

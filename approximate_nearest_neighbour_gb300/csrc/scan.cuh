@@ -134,18 +134,14 @@ __device__ __forceinline__ float lut_load(const char* addr) {
 template <int MW, int LT>
 __device__ __forceinline__ float adc_sum(const uint32_t (&w)[MW], const char* lut_bytes,
                                          uint32_t lane4) {
-  float acc0 = 0.f, acc1 = 0.f;
+  // four independent accumulation chains keep the adds off the critical path
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int s = 0; s < 4 * MW; ++s) {
     const uint32_t off = __byte_perm(w[s >> 2], lane4, 0x5504u | (uint32_t(s & 3) << 4));
-    const float v =
-        lut_load<LT>(lut_bytes + off + ((s >> 5) * kGroupWords + (s & 31)) * 4);
-    if (s & 1)
-      acc1 += v;
-    else
-      acc0 += v;
+    acc[s & 3] += lut_load<LT>(lut_bytes + off + ((s >> 5) * kGroupWords + (s & 31)) * 4);
   }
-  return acc0 + acc1;
+  return (acc[0] + acc[1]) + (acc[2] + acc[3]);
 }
 
 // Converts the fp32 tables in place to the storage type (all words of the

@@ -1,0 +1,166 @@
+// List scan with the codebook held in registers and double-buffered tables.
+//
+// Same computation as ivfpq_scan_kernel (scan.cuh; sources: "Billion-scale
+// similarity search with GPUs", section 5, tables T_1..T_b and their use in
+// the list scan; "Custom 8-bit floating point value format ...", search steps
+// 2-5 and Eq. (1)), organised for the shapes where it pays:
+//  * 16 warps per block, one block per SM (two 64 KB table buffers);
+//  * the 256 x m codewords (d floats each row) are split over the 512
+//    threads and kept in registers for the whole block (d/2 floats per
+//    thread), so building a table reads no memory but the centroid: thread
+//    (warp w, lane i) owns sub-quantizer jj = i mod GS of the group and the
+//    reproduction values e = (s*16 + w) * QQ + i / GS, QQ = 32 / GS;
+//  * the table of list i+1 is built into one buffer while list i is scanned
+//    with the other, so each probed list costs one block barrier.
+// The shared-memory table layout, the rotated code layout, the look-up
+// addressing and the selection are those of scan.cuh.
+#pragma once
+
+#include "scan.cuh"
+
+namespace ivfpq {
+
+constexpr int kScan2Warps = 16;
+
+template <int MW, int DS>
+struct Scan2Shape {
+  static constexpr int M = 4 * MW;
+  static_assert(M <= 32, "one group of sub-quantizers");
+  static constexpr int GS = M;  // group size: all sub-quantizers
+  static constexpr int QQ = 32 / GS;
+  static constexpr int LOG_GS = GS == 32 ? 5 : GS == 16 ? 4 : GS == 8 ? 3 : 2;
+  static constexpr int STEPS = 256 / (kScan2Warps * QQ);  // values per thread
+  static constexpr int REPS = 64 / GS;                     // copies of a table in a row
+  static constexpr int DS4 = (DS + 3) & ~3;
+};
+
+template <int MW, int DS, int K>
+__global__ void __launch_bounds__(kScan2Warps * 32, 1)
+ivfpq_scan2_kernel(const ScanParams p) {
+  using Sh = Scan2Shape<MW, DS>;
+  constexpr int T = ThreadQ<K>::value;
+  constexpr int NW = kScan2Warps;
+  constexpr int m = Sh::M;
+  extern __shared__ __align__(16) uint32_t scan2_smem[];
+  float* buf0 = reinterpret_cast<float*>(scan2_smem);
+  float* buf1 = buf0 + kGroupWords;
+
+  const int64_t q = int64_t(blockIdx.x) / p.nchunks;
+  const int chunk = int(int64_t(blockIdx.x) % p.nchunks);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int jj = lane & (Sh::GS - 1), qq = lane >> Sh::LOG_GS;
+
+  // this thread's codewords and query slice
+  float cw[Sh::STEPS][DS];
+#pragma unroll
+  for (int s = 0; s < Sh::STEPS; ++s) {
+    const int e = (s * NW + warp) * Sh::QQ + qq;
+    const float* c = p.codebooks_t + (int64_t(e) * m + jj) * Sh::DS4;
+#pragma unroll
+    for (int t = 0; t < DS; ++t) cw[s][t] = __ldg(c + t);
+  }
+  float xs[DS];
+  const float* x = p.queries + q * p.d + jj * DS;
+#pragma unroll
+  for (int t = 0; t < DS; ++t) xs[t] = __ldg(x + t);
+
+  // table of list l into buf (fp32 entries, one per 4-byte slot)
+  auto build = [&](int l, float* buf) {
+    const float* cl = p.centroids + int64_t(l) * p.d + jj * DS;
+    float r[DS];
+#pragma unroll
+    for (int t = 0; t < DS; ++t) r[t] = xs[t] - __ldg(cl + t);
+#pragma unroll
+    for (int s = 0; s < Sh::STEPS; ++s) {
+      const int e = (s * NW + warp) * Sh::QQ + qq;
+      float Tv = 0.f;
+#pragma unroll
+      for (int t = 0; t < DS; ++t) {
+        const float df = r[t] - cw[s][t];
+        Tv = fmaf(df, df, Tv);
+      }
+      float* row = buf + e * 64 + jj;
+#pragma unroll
+      for (int rep = 0; rep < Sh::REPS; ++rep)
+        row[Sh::GS * ((rep + qq) & (Sh::REPS - 1))] = Tv;
+    }
+  };
+
+  WarpSelect<K, T> ws;
+  ws.init(lane);
+  const int p0 = chunk * p.per_chunk;
+  const int p1 = min(p.nprobe, p0 + p.per_chunk);
+  const int32_t* qprobes = p.probes + q * p.nprobe;
+  const uint32_t lane4 = uint32_t(lane) * 4;
+  auto valid_list = [&](int l) { return l >= 0 && l < p.nlist; };
+
+  if (tid == 0 && p0 < p1) prefetch_list(p, qprobes[p0], m);
+  if (p0 < p1 && valid_list(qprobes[p0])) build(qprobes[p0], buf0);
+  __syncthreads();
+
+  for (int pi = p0; pi < p1; ++pi) {
+    const int l = qprobes[pi];
+    float* cur = ((pi - p0) & 1) ? buf1 : buf0;
+    float* nxt = ((pi - p0) & 1) ? buf0 : buf1;
+    if (pi + 1 < p1) {
+      const int ln = qprobes[pi + 1];
+      if (tid == 0) prefetch_list(p, ln, m);
+      if (valid_list(ln)) build(ln, nxt);
+    }
+    if (valid_list(l)) {
+      const int len = p.list_len[l];
+      const int64_t boff = p.list_block_off[l];
+      const int nb = (len + 31) >> 5;
+      const uint8_t* lcodes = p.codes + boff * 32 * m;
+      const char* lut_bytes = reinterpret_cast<const char*>(cur);
+      uint32_t c0[MW], c1[MW];
+      int b = warp;
+      if (b < nb) load_codes<MW>(lcodes + int64_t(b) * 32 * m, lane, c0);
+      for (; b < nb; b += NW) {
+        const int bn = b + NW;
+        if (bn < nb) load_codes<MW>(lcodes + int64_t(bn) * 32 * m, lane, c1);
+        const float dist = adc_sum<MW, IVFPQ_LUT_FP32>(c0, lut_bytes, lane4);
+        const bool valid = b * 32 + lane < len;
+        ws.add(valid ? __float_as_uint(dist) : kSentinelKey, uint32_t((boff + b) * 32 + lane));
+#pragma unroll
+        for (int w = 0; w < MW; ++w) c0[w] = c1[w];
+      }
+    }
+    __syncthreads();  // cur may be overwritten next; nxt is complete
+  }
+  ws.finalize();
+  block_merge<K, T, NW>(ws, scan2_smem, scan2_smem + NW * K, warp);
+  if (warp == 0) {
+    const int64_t o = (q * p.nchunks + chunk) * p.k;
+#pragma unroll
+    for (int r = 0; r < K / 32; ++r) {
+      const int i = 32 * r + lane;
+      if (i < p.k) {
+        p.pkeys[o + i] = ws.wk[r];
+        p.pidx[o + i] = ws.wv[r];
+      }
+    }
+  }
+}
+
+inline size_t scan2_smem_bytes(int K) {
+  const size_t luts = size_t(2) * kGroupWords * 4;
+  const size_t merge = size_t(kScan2Warps) * K * 8;
+  return luts > merge ? luts : merge;
+}
+
+template <int MW, int DS, int K>
+int launch_scan2(const ScanParams& p, int64_t nq, cudaStream_t s) {
+  auto kern = ivfpq_scan2_kernel<MW, DS, K>;
+  const size_t smem = scan2_smem_bytes(K);
+  IVFPQ_TRY(set_dynamic_smem(kern, smem));
+  const int64_t blocks = nq * p.nchunks;
+  kern<<<unsigned(blocks), kScan2Warps * 32, smem, s>>>(p);
+  IVFPQ_LAUNCHED_K(kern, smem, kScan2Warps * 32);
+  return IVFPQ_OK;
+}
+
+}  // namespace ivfpq
+
+#define IVFPQ_INST_SCAN2(MW, DS, K) \
+  template int ivfpq::launch_scan2<MW, DS, K>(const ivfpq::ScanParams&, int64_t, cudaStream_t);
