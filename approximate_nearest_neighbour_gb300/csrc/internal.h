@@ -50,11 +50,29 @@ int kselect_device(const float* vals, int64_t rows, int64_t cols, int k, const S
 int l2_distance_tile(const float* Q, int64_t nq, const float* X, int64_t n, int d, float* D,
                      int64_t ldd, cudaStream_t s);
 
+// ---- tensor-core distance tiles (gemm_tc.cu) -------------------------------------
+// Operands for 3xTF32 distances: hi/lo split rows padded to tc_dpad(d) columns
+// and fp32 squared norms.
+struct TcOperand {
+  const float* hi = nullptr;
+  const float* lo = nullptr;
+  const float* norms = nullptr;
+};
+bool l2_tc_available(int d);
+int tc_dpad(int d);
+int l2_tc_prepare(const float* x, int64_t rows, int d, float* hi, float* lo, float* norms,
+                  cudaStream_t s);
+// D[i*ldd + j] = ||q_i||^2 + ||x_j||^2 - 2 <q_i, x_j> (3xTF32) for i < nq, j < n.
+int l2_tc_tiles(const float* qhi, const float* qlo, const float* qnorm, int64_t nq,
+                const float* xhi, const float* xlo, const float* xnorm, int64_t n, int d,
+                float* D, int64_t ldd, int* err, cudaStream_t s);
+
 // ---- flat / coarse search on distance tiles (flat.cu) ----------------------------
 // k nearest rows of X for each row of Q under squared L2; output as SelectOut
 // (Float with column ids, or Probes).
+// xop: precomputed tensor-core operands of X (may be null).
 int knn_by_tiles(const float* Q, int64_t nq, const float* X, int64_t n, int d, int k,
-                 const SelectOut& out, cudaStream_t s);
+                 const SelectOut& out, cudaStream_t s, const TcOperand* xop = nullptr);
 
 }  // namespace ivfpq
 
@@ -66,6 +84,9 @@ struct ivfpq_index {
   float* centroids = nullptr;   // [nlist, d]
   float* cent_norms = nullptr;  // [nlist]
   float* codebooks = nullptr;   // [256, m, dsub4], zero-padded to dsub4 = roundup(dsub, 4)
+  // tensor-core operands of the centroids (null when that path is unavailable)
+  float* cent_hi = nullptr;     // [nlist, tc_dpad(d)]
+  float* cent_lo = nullptr;
   // inverted lists, interleaved in blocks of 32 vectors
   int64_t ntotal = 0;
   int64_t nblocks = 0;

@@ -195,6 +195,16 @@ extern "C" int ivfpq_index_create(int d, int nlist, int m, int nbits, const floa
   transpose_codebooks_kernel<<<grid_for(int64_t(cb4_n), 256), 256, 0, 0>>>(
       cb_tmp, m, ix->dsub, ix->dsub4, ix->codebooks);
   CREATE_CUDA(cudaGetLastError());
+  if (l2_tc_available(d)) {
+    const size_t nn = size_t(nlist) * tc_dpad(d);
+    CREATE_CUDA(cudaMalloc(&ix->cent_hi, nn * sizeof(float)));
+    CREATE_CUDA(cudaMalloc(&ix->cent_lo, nn * sizeof(float)));
+    const int st = l2_tc_prepare(ix->centroids, nlist, d, ix->cent_hi, ix->cent_lo, ix->cent_norms, 0);
+    if (st != IVFPQ_OK) {
+      cudaFree(cb_tmp);
+      return fail(st);
+    }
+  }
   CREATE_CUDA(cudaStreamSynchronize(0));
   cudaFree(cb_tmp);
   cb_tmp = nullptr;
@@ -209,6 +219,8 @@ extern "C" int ivfpq_index_destroy(ivfpq_index* ix) {
   cudaDeviceSynchronize();
   cudaFree(ix->centroids);
   cudaFree(ix->cent_norms);
+  cudaFree(ix->cent_hi);
+  cudaFree(ix->cent_lo);
   cudaFree(ix->codebooks);
   cudaFree(ix->list_len);
   cudaFree(ix->list_block_off);

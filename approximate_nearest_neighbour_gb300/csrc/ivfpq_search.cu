@@ -134,7 +134,12 @@ int coarse_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int np
   o.kind = OutKind::Probes;
   o.idx32 = probes;
   o.vals = coarse;
-  return knn_by_tiles(queries, nq, ix->centroids, ix->nlist, ix->d, nprobe, o, s);
+  TcOperand xo;
+  xo.hi = ix->cent_hi;
+  xo.lo = ix->cent_lo;
+  xo.norms = ix->cent_norms;
+  return knn_by_tiles(queries, nq, ix->centroids, ix->nlist, ix->d, nprobe, o, s,
+                      ix->cent_hi ? &xo : nullptr);
 }
 
 // Lists per block: enough blocks to give every SM several waves.

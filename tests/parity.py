@@ -34,7 +34,8 @@ def compare_knn(gd, gi, od, oi, rtol=RTOL, atol=ATOL, context=""):
         g = gd[r]
         fin = np.isfinite(D)
         t = np.maximum(rtol * np.abs(D), atol)
-        bad = np.nonzero(fin & ~(np.abs(g - D) <= t))[0]
+        diff = np.abs(np.where(fin, g, 0.0) - np.where(fin, D, 0.0))
+        bad = np.nonzero(fin & ~(diff <= t))[0]
         assert bad.size == 0, f"{context} row {r}: distance mismatch at ranks {bad[:8]}: " \
                               f"gpu {g[bad[:4]]} oracle {D[bad[:4]]}"
         assert np.all(np.isinf(g[~fin])), f"{context} row {r}: missing results must be +inf"
