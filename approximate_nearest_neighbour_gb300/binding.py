@@ -46,6 +46,8 @@ SIGNATURES = {
     "flat_knn": (_I, [_VP, _I64, _I, _VP, _I64, _I, _VP, _VP, _VP]),
     "kselect": (_I, [_VP, _I64, _I64, _I, _VP, _VP, _VP]),
     "kselect_noalloc": (_I, [_VP, _I64, _I64, _I, _VP, _VP, _VP]),
+    "ivfpq_device_check": (_I, [_VP]),
+    "ivfpq_selftest_wait_timeout": (_I, [_I, _VP]),
     "ivfpq_last_error": (C.c_char_p, []),
     "ivfpq_status_string": (C.c_char_p, [_I]),
 }
@@ -241,6 +243,20 @@ def ivfpq_stage_times(index):
 def kernel_launches():
     """Kernels launched by the library since it was loaded."""
     return int(lib().ivfpq_kernel_launches())
+
+
+def device_check(stream=None):
+    """Synchronises the stream and raises IVFPQError (IVFPQ_ERR_TIMEOUT) if a
+    kernel of the library gave up a bounded wait since the last check."""
+    _check("ivfpq_device_check", lib().ivfpq_device_check(_stream(stream)))
+
+
+def selftest_wait_timeout(spins=1024, stream=None):
+    """Launches a block whose bounded wait is bound to expire (nothing
+    completes the barrier phase it waits on); device_check() then reports
+    it."""
+    _check("ivfpq_selftest_wait_timeout",
+           lib().ivfpq_selftest_wait_timeout(int(spins), _stream(stream)))
 
 
 def flat_knn(db, queries, k, out_dist=None, out_ids=None, stream=None):

@@ -2,6 +2,7 @@
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -21,7 +22,46 @@ void clear_error() { g_err[0] = 0; }
 static std::atomic<unsigned long long> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+// One status word per device, allocated on first use and kept while the
+// library is loaded. Kernels whose bounded waits expire set it to 1.
+static std::mutex g_status_mu;
+static int* g_status[64] = {};
+
+int device_status_word(int** out) {
+  int dev = 0;
+  IVFPQ_CUDA(cudaGetDevice(&dev));
+  IVFPQ_REQUIRE(dev >= 0 && dev < 64, "device %d not supported", dev);
+  std::lock_guard<std::mutex> lock(g_status_mu);
+  if (!g_status[dev]) {
+    int* p = nullptr;
+    IVFPQ_CUDA(cudaMalloc(&p, sizeof(int)));
+    IVFPQ_CUDA(cudaMemset(p, 0, sizeof(int)));
+    g_status[dev] = p;
+  }
+  *out = g_status[dev];
+  return IVFPQ_OK;
+}
+
 }  // namespace ivfpq
+
+extern "C" int ivfpq_device_check(void* stream) {
+  using namespace ivfpq;
+  clear_error();
+  int* w = nullptr;
+  IVFPQ_TRY(device_status_word(&w));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int h = 0;
+  IVFPQ_CUDA(cudaMemcpyAsync(&h, w, sizeof(int), cudaMemcpyDeviceToHost, s));
+  IVFPQ_CUDA(cudaStreamSynchronize(s));
+  if (h != 0) {
+    IVFPQ_CUDA(cudaMemsetAsync(w, 0, sizeof(int), s));
+    IVFPQ_CUDA(cudaStreamSynchronize(s));
+    set_error("a kernel's bounded wait expired: results of the calls since the last check "
+              "are invalid");
+    return IVFPQ_ERR_TIMEOUT;
+  }
+  return IVFPQ_OK;
+}
 
 extern "C" const char* ivfpq_last_error(void) { return ivfpq::g_err; }
 

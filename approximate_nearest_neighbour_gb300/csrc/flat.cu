@@ -47,21 +47,76 @@ __global__ void rerank_kernel(const float* __restrict__ Q, const float* __restri
 // Bytes of distance workspace per query tile.
 static const int64_t kTileBytes = int64_t(2) << 30;
 
+namespace {
+
+// Re-ranks the k selected entries of each row of o in the exact direct form
+// and re-sorts them (scratch: 2 * rows * k words). The GEMM form loses
+// absolute precision ~eps * (|q|^2 + |x|^2) to cancellation.
+int rerank(const float* Q, const float* X, int d, int64_t rows, int k, const SelectOut& o,
+           uint32_t* scratch, cudaStream_t s) {
+  uint32_t* rk = scratch;
+  uint32_t* rc = rk + rows * k;
+  const int64_t warps = rows * k;
+  rerank_kernel<<<unsigned(ceil_div(warps * 32, 256)), 256, 0, s>>>(
+      Q, X, d, rows, k, o.idx64, o.kind == OutKind::Probes ? o.idx32 : nullptr, rk, rc);
+  IVFPQ_LAUNCHED();
+  return select_pairs(rk, rc, rows, k, k, 1, k, o, s);
+}
+
+// Filtered plan (k <= 256, large n). A first tensor-core pass over the
+// first ns columns takes, per row, the minimum of u = D - ||q||^2 over each of
+// G >= 4k column groups; the k-th smallest of those G minima is an upper
+// bound on the row's k-th smallest u over all n columns (it is attained by k
+// distinct columns). The full pass then keeps only entries at or below it:
+// about k * n / ns of them per row, instead of writing and re-reading the
+// whole distance row.
+struct FilterPlan {
+  int64_t ns = 0;   // columns of the first pass
+  int split_a = 0;  // CTAs per query tile in the first pass (G = 128 * split_a)
+};
+
+bool filter_plan(int64_t n, int k, FilterPlan* fp) {
+  if (k > 256 || n < 16384) return false;
+  const int64_t ns = ceil_div(ceil_div(n, 8), 128) * 128;
+  const int split_a = int(ceil_div(4 * int64_t(k), 128));
+  if (ns / 128 < split_a || 2 * ns > n) return false;
+  fp->ns = ns;
+  fp->split_a = split_a;
+  return true;
+}
+
+SelectOut offset_out(const SelectOut& out, int64_t off) {
+  SelectOut o = out;
+  if (o.vals) o.vals += off;
+  if (o.idx64) o.idx64 += off;
+  if (o.idx32) o.idx32 += off;
+  return o;
+}
+
+}  // namespace
+
 int knn_by_tiles(const float* Q, int64_t nq, const float* X, int64_t n, int d, int k,
                  const SelectOut& out, cudaStream_t s, const TcOperand* xop) {
   if (nq == 0) return IVFPQ_OK;
-  int64_t tq = std::max<int64_t>(128, kTileBytes / (4 * std::max<int64_t>(n, 1)) / 128 * 128);
-  tq = std::min(std::min(tq, nq), int64_t(65535) * 128);
   Workspace ws(s);
-  float* D = nullptr;
   const bool tc = n > 0 && l2_tc_available(d);
-  // the re-rank pairs (2 words per selected entry) reuse the distance tile
-  const int64_t tile_words = std::max<int64_t>(n, tc ? 2 * int64_t(k) : 1);
-  IVFPQ_TRY(ws.alloc(&D, size_t(tq * tile_words)));
+  if (!tc) {
+    int64_t tq = std::max<int64_t>(128, kTileBytes / (4 * std::max<int64_t>(n, 1)) / 128 * 128);
+    tq = std::min(std::min(tq, nq), int64_t(65535) * 128);
+    float* D = nullptr;
+    IVFPQ_TRY(ws.alloc(&D, size_t(tq * std::max<int64_t>(n, 1))));
+    for (int64_t q0 = 0; q0 < nq; q0 += tq) {
+      const int64_t rows = std::min(tq, nq - q0);
+      if (n > 0) IVFPQ_TRY(l2_distance_tile(Q + q0 * d, rows, X, n, d, D, n, s));
+      IVFPQ_TRY(kselect_device(D, rows, n, k, offset_out(out, q0 * k), s));
+    }
+    return IVFPQ_OK;
+  }
+
+  // tensor-core operands
+  const int dpad = tc_dpad(d);
   TcOperand qo, xo;
-  int* err = nullptr;
-  if (tc) {
-    const int dpad = tc_dpad(d);
+  {
     float *qhi, *qlo, *qn;
     IVFPQ_TRY(ws.alloc(&qhi, size_t(nq) * dpad));
     IVFPQ_TRY(ws.alloc(&qlo, size_t(nq) * dpad));
@@ -70,48 +125,85 @@ int knn_by_tiles(const float* Q, int64_t nq, const float* X, int64_t n, int d, i
     qo.hi = qhi;
     qo.lo = qlo;
     qo.norms = qn;
-    if (xop) {
-      xo = *xop;
-    } else {
-      float *xhi, *xlo, *xn;
-      IVFPQ_TRY(ws.alloc(&xhi, size_t(n) * dpad));
-      IVFPQ_TRY(ws.alloc(&xlo, size_t(n) * dpad));
-      IVFPQ_TRY(ws.alloc(&xn, size_t(n)));
-      IVFPQ_TRY(l2_tc_prepare(X, n, d, xhi, xlo, xn, s));
-      xo.hi = xhi;
-      xo.lo = xlo;
-      xo.norms = xn;
-    }
-    IVFPQ_TRY(ws.alloc(&err, 1));
-    IVFPQ_CUDA(cudaMemsetAsync(err, 0, sizeof(int), s));
   }
+  if (xop) {
+    xo = *xop;
+  } else {
+    float *xhi, *xlo, *xn;
+    IVFPQ_TRY(ws.alloc(&xhi, size_t(n) * dpad));
+    IVFPQ_TRY(ws.alloc(&xlo, size_t(n) * dpad));
+    IVFPQ_TRY(ws.alloc(&xn, size_t(n)));
+    IVFPQ_TRY(l2_tc_prepare(X, n, d, xhi, xlo, xn, s));
+    xo.hi = xhi;
+    xo.lo = xlo;
+    xo.norms = xn;
+  }
+  int* err = nullptr;
+  IVFPQ_TRY(device_status_word(&err));
+
+  FilterPlan fp;
+  if (filter_plan(n, k, &fp)) {
+    const int64_t G = 128 * int64_t(fp.split_a);
+    // candidate segments: nseg per row from the filter pass's CTA split, each
+    // holding 4x its expected share of ~1.5 k n / ns survivors (at least 64)
+    auto seg_cap = [&](int nseg) {
+      const int64_t expect = ceil_div(3 * int64_t(k) * n, 2 * fp.ns);
+      return int(ceil_div(std::max<int64_t>(64, ceil_div(4 * expect, nseg)), 32) * 32);
+    };
+    int64_t tq = std::min(nq, int64_t(65535) * 128);
+    for (;;) {
+      const int nseg = 2 * tc_filter_split(tq, n);
+      const int64_t row_bytes = G * 4 + int64_t(k) * 12 + int64_t(nseg) * (seg_cap(nseg) * 8 + 4);
+      if (tq <= 128 || tq * row_bytes <= kTileBytes) break;
+      tq = std::max<int64_t>(128, (tq / 2) / 128 * 128);
+    }
+    const int split_b = tc_filter_split(tq, n);
+    const int nseg = 2 * split_b;
+    const int cap_s = seg_cap(nseg);
+    float* gmin = nullptr;
+    float* tv = nullptr;
+    int64_t* ti = nullptr;
+    uint64_t* cand = nullptr;
+    int* scnt = nullptr;
+    IVFPQ_TRY(ws.alloc(&gmin, size_t(tq * G)));
+    IVFPQ_TRY(ws.alloc(&tv, size_t(tq * k)));
+    IVFPQ_TRY(ws.alloc(&ti, size_t(tq * k)));
+    IVFPQ_TRY(ws.alloc(&cand, size_t(tq * nseg) * cap_s));
+    IVFPQ_TRY(ws.alloc(&scnt, size_t(tq * nseg)));
+    for (int64_t q0 = 0; q0 < nq; q0 += tq) {
+      const int64_t rows = std::min(tq, nq - q0);
+      IVFPQ_TRY(l2_tc_group_min(qo.hi + q0 * dpad, qo.lo + q0 * dpad, rows, xo.hi, xo.lo,
+                                xo.norms, fp.ns, d, fp.split_a, gmin, err, s));
+      SelectOut first;
+      first.kind = OutKind::Float;
+      first.vals = tv;
+      first.idx64 = ti;
+      IVFPQ_TRY(select_rows(gmin, rows, G, k, 1, G, first, s));
+      IVFPQ_TRY(l2_tc_filter(qo.hi + q0 * dpad, qo.lo + q0 * dpad, qo.norms + q0, rows, xo.hi,
+                             xo.lo, xo.norms, n, d, tv + (k - 1), k, split_b, cand, scnt, cap_s,
+                             err, s));
+      const SelectOut o = offset_out(out, q0 * k);
+      IVFPQ_TRY(
+          select_candidates(cand, scnt, nseg, cap_s, rows, Q + q0 * d, X, n, d, k, o, s));
+      // G >= 4k words per row hold the re-rank pairs
+      IVFPQ_TRY(rerank(Q + q0 * d, X, d, rows, k, o, reinterpret_cast<uint32_t*>(gmin), s));
+    }
+    return IVFPQ_OK;
+  }
+
+  int64_t tq = std::max<int64_t>(128, kTileBytes / (4 * std::max<int64_t>(n, 1)) / 128 * 128);
+  tq = std::min(std::min(tq, nq), int64_t(65535) * 128);
+  // the re-rank pairs (2 words per selected entry) reuse the distance tile
+  const int64_t tile_words = std::max<int64_t>(n, 2 * int64_t(k));
+  float* D = nullptr;
+  IVFPQ_TRY(ws.alloc(&D, size_t(tq * tile_words)));
   for (int64_t q0 = 0; q0 < nq; q0 += tq) {
     const int64_t rows = std::min(tq, nq - q0);
-    if (tc) {
-      const int dpad = tc_dpad(d);
-      IVFPQ_TRY(l2_tc_tiles(qo.hi + q0 * dpad, qo.lo + q0 * dpad, qo.norms + q0, rows, xo.hi,
-                            xo.lo, xo.norms, n, d, D, n, err, s));
-    } else {
-      IVFPQ_TRY(l2_distance_tile(Q + q0 * d, rows, X, n, d, D, n, s));
-    }
-    SelectOut o = out;
-    if (o.vals) o.vals += q0 * k;
-    if (o.idx64) o.idx64 += q0 * k;
-    if (o.idx32) o.idx32 += q0 * k;
+    IVFPQ_TRY(l2_tc_tiles(qo.hi + q0 * dpad, qo.lo + q0 * dpad, qo.norms + q0, rows, xo.hi, xo.lo,
+                          xo.norms, n, d, D, n, err, s));
+    const SelectOut o = offset_out(out, q0 * k);
     IVFPQ_TRY(kselect_device(D, rows, n, k, o, s));
-    if (tc) {
-      // The GEMM form loses absolute precision ~eps * (|q|^2 + |x|^2) to
-      // cancellation; the winners' distances are recomputed in the direct
-      // form and re-sorted.
-      uint32_t* rk = reinterpret_cast<uint32_t*>(D);
-      uint32_t* rc = rk + rows * k;
-      const int64_t warps = rows * k;
-      rerank_kernel<<<unsigned(ceil_div(warps * 32, 256)), 256, 0, s>>>(
-          Q + q0 * d, X, d, rows, k, o.idx64, o.kind == OutKind::Probes ? o.idx32 : nullptr, rk,
-          rc);
-      IVFPQ_LAUNCHED();
-      IVFPQ_TRY(select_pairs(rk, rc, rows, k, k, 1, k, o, s));
-    }
+    IVFPQ_TRY(rerank(Q + q0 * d, X, d, rows, k, o, reinterpret_cast<uint32_t*>(D), s));
   }
   return IVFPQ_OK;
 }

@@ -9,7 +9,7 @@
 // quantizer ("Billion-scale similarity search with GPUs", section 5, exact
 // search; "Faiss GPU: k-select that never leaves registers", Step 5).
 //
-// Kernel organisation (one CTA per SM, 6 warps):
+// Kernel organisation (one CTA per SM, 10 warps):
 //  * warp 0, one thread: TMA producer. Loads the CTA's 128-query tile of
 //    q_hi / q_lo once (all of K), then streams 128-row tiles of x_hi / x_lo
 //    through an NSTAGE ring, one 32-column (128-byte, 128B-swizzled) K chunk
@@ -18,8 +18,12 @@
 //    and, one thread, issues tcgen05.mma kind::tf32 (M = 128, N = 128, K = 8)
 //    three times per K step, committing stage releases and finished
 //    accumulators to mbarriers;
-//  * warps 2..5: epilogue. Thread t of the four warps owns TMEM lane (query
-//    row) t; it reads its row with tcgen05.ld, adds the norms and writes D.
+//  * warps 2..9: epilogue. Thread t of warps w and w + 4 owns TMEM lane
+//    (query row) 32 * (w % 4) + t, one warp of the pair the first 64
+//    accumulator columns, the other the last 64. Three modes: write D; keep
+//    per-row minima over column groups; or keep only the entries at or below
+//    a per-row bound, appended to the (row, CTA, half) segment of a candidate
+//    buffer with a register counter (no atomics).
 // Every mbarrier wait is bounded: on expiry the CTA records an error in
 // *err, stops issuing work, waits (bounded) for its copies and MMAs in
 // flight, frees its TMEM and returns.
@@ -55,8 +59,9 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 // Waits for the phase of the given parity to complete; false after the spin
 // limit.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          uint32_t limit = kSpinLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     uint32_t done;
     asm volatile(
         "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
@@ -119,15 +124,36 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+enum TcMode : int {
+  kModeTile = 0,      // write D
+  kModeGroupMin = 1,  // per-row minima of u over column groups
+  kModeFilter = 2     // per-row candidate segments of entries with u <= bound
+};
+
+// u[i, j] = ||x_j||^2 - 2 <q_i, x_j> = D[i, j] - ||q_i||^2 (the same order per
+// row as D); the filter and group-minimum modes work on u.
 struct TcArgs {
   const float* qnorm;  // [nq]
   const float* xnorm;  // [n]
-  float* D;            // [nq, ldd]
-  int64_t ldd;
   int nq, n;
   int ntiles_n;        // ceil(n / TN)
-  int nsplit;          // CTAs per query tile
+  int nsplit;          // CTAs per query tile (contiguous runs of column tiles)
   int* err;
+  // tile mode
+  float* D;            // [nq, ldd]
+  int64_t ldd;
+  // group-minimum mode: gmin[i * G + split * TN + c] = min over the CTA's
+  // columns j = c (mod TN) of u[i, j], G = nsplit * TN (+inf if none)
+  float* gmin;
+  // filter mode: entries with u[i, j] <= bound[i * bound_stride] (widened by
+  // a few ulps) go to segment (i, split * 2 + half) of cap_s packed
+  // (key of D << 32 | j) entries, half = which 64 columns of each tile;
+  // scnt[i * nseg + seg] = entries found (may exceed cap_s: overflow).
+  const float* bound;
+  int64_t bound_stride;
+  uint64_t* cand;
+  int* scnt;
+  int cap_s;
 };
 
 template <int KC, int NSTAGE>
@@ -138,8 +164,11 @@ struct TcSmem {
   static constexpr int kTotal = kA + kB + kBars + 1024;  // + alignment slack
 };
 
-template <int KC, int NSTAGE>
-__global__ void __launch_bounds__(192, 1)
+constexpr int kEpiWarps = 8;                    // two per TMEM lane group
+constexpr int kTcThreads = (2 + kEpiWarps) * 32;  // producer, MMA, epilogue
+
+template <int KC, int NSTAGE, int MODE>
+__global__ void __launch_bounds__(kTcThreads, 1)
 l2_tc_kernel(const __grid_constant__ CUtensorMap mq_hi, const __grid_constant__ CUtensorMap mq_lo,
              const __grid_constant__ CUtensorMap mx_hi, const __grid_constant__ CUtensorMap mx_lo,
              const TcArgs a) {
@@ -176,7 +205,7 @@ l2_tc_kernel(const __grid_constant__ CUtensorMap mq_hi, const __grid_constant__ 
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_accf(b), 1);
-      mbar_init(bar_acce(b), 4);
+      mbar_init(bar_acce(b), kEpiWarps);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -267,13 +296,30 @@ l2_tc_kernel(const __grid_constant__ CUtensorMap mq_hi, const __grid_constant__ 
     // on an early exit, let the issued MMAs finish before TMEM is freed
     if (committed > 0) mbar_wait(bar_accf((committed - 1) & 1), ((committed - 1) >> 1) & 1);
   } else if (warp >= 2) {
-    // ---- epilogue ----
-    const int lg = warp & 3;  // TMEM lane group this warp may access
+    // ---- epilogue: warp w reads TMEM lanes 32 * (w % 4) .. +32 (its rows)
+    // and the 64 accumulator columns of its half ----
+    const int lg = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row = 32 * lg + lane;
     const int q = qt * TM + row;
-    const float qn = q < a.nq ? __ldg(a.qnorm + q) : 0.f;
-    float* drow = a.D + int64_t(q) * a.ldd;
-    const bool vec = (a.ldd % 4) == 0 && ((reinterpret_cast<uintptr_t>(a.D) & 15) == 0);
+    const bool live = q < a.nq;
+    const float qn = live ? __ldg(a.qnorm + q) : 0.f;
+    constexpr int NC = TN / 32 / 2;  // 32-column chunks per half
+    float gm[MODE == kModeGroupMin ? NC * 32 : 1];
+    if constexpr (MODE == kModeGroupMin) {
+#pragma unroll
+      for (int j = 0; j < NC * 32; ++j) gm[j] = INFINITY;
+    }
+    float bnd = -INFINITY;  // rows past nq keep nothing
+    int cnt = 0;
+    uint64_t* seg = nullptr;
+    if constexpr (MODE == kModeFilter) {
+      if (live) {
+        const float t = __ldg(a.bound + int64_t(q) * a.bound_stride);
+        bnd = t + fabsf(t) * 1e-6f;
+      }
+      seg = a.cand + (int64_t(q) * (2 * a.nsplit) + 2 * split + half) * a.cap_s;
+    }
     for (int i = 0; i < ntiles && !*abort_flag; ++i) {
       const int ab = i & 1;
       if (!mbar_wait(bar_accf(ab), (i >> 1) & 1)) {
@@ -282,33 +328,63 @@ l2_tc_kernel(const __grid_constant__ CUtensorMap mq_hi, const __grid_constant__ 
       }
       tc_fence_after();
       const int col0 = (t0 + i) * TN;
-#pragma unroll 1
-      for (int c = 0; c < TN / 32; ++c) {
+#pragma unroll
+      for (int cc = 0; cc < NC; ++cc) {
+        const int c = half * NC + cc;
         float v[32];
         tmem_ld32(tmem + (uint32_t(32 * lg) << 16) + uint32_t(ab * TN + c * 32), v);
         const int cb = col0 + c * 32;
+        float xn[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int col = cb + j;
-          const float xn = col < a.n ? __ldg(a.xnorm + col) : 0.f;
-          v[j] = fmaf(-2.f, v[j], qn + xn);
-        }
-        if (q < a.nq) {
-          if (vec && cb + 32 <= a.n) {
-            float4* o = reinterpret_cast<float4*>(drow + cb);
+        for (int j = 0; j < 32; ++j) xn[j] = cb + j < a.n ? __ldg(a.xnorm + cb + j) : 0.f;
+        if constexpr (MODE == kModeTile) {
+          float* drow = a.D + int64_t(q) * a.ldd;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-          } else {
+          for (int j = 0; j < 32; ++j) v[j] = fmaf(-2.f, v[j], qn + xn[j]);
+          if (live) {
+            const bool vec = (a.ldd % 4) == 0 && ((reinterpret_cast<uintptr_t>(a.D) & 15) == 0);
+            if (vec && cb + 32 <= a.n) {
+              float4* o = reinterpret_cast<float4*>(drow + cb);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (cb + j < a.n) drow[cb + j] = v[j];
+              for (int j = 0; j < 8; ++j)
+                o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (cb + j < a.n) drow[cb + j] = v[j];
+            }
+          }
+        } else if constexpr (MODE == kModeGroupMin) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float u = fmaf(-2.f, v[j], xn[j]);
+            if (cb + j < a.n) gm[cc * 32 + j] = fminf(gm[cc * 32 + j], u);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float u = fmaf(-2.f, v[j], xn[j]);
+            if (u <= bnd && cb + j < a.n) {
+              if (cnt < a.cap_s)
+                seg[cnt] = (uint64_t(float_to_key(u + qn)) << 32) | uint32_t(cb + j);
+              ++cnt;
+            }
           }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_acce(ab));
+    }
+    if constexpr (MODE == kModeGroupMin) {
+      if (live) {
+        float* g = a.gmin + int64_t(q) * (int64_t(a.nsplit) * TN) + split * TN + half * NC * 32;
+#pragma unroll
+        for (int j = 0; j < NC * 32; ++j) g[j] = gm[j];
+      }
+    }
+    if constexpr (MODE == kModeFilter) {
+      if (live) a.scnt[int64_t(q) * (2 * a.nsplit) + 2 * split + half] = cnt;
     }
   }
   tc_fence_before();
@@ -318,6 +394,17 @@ l2_tc_kernel(const __grid_constant__ CUtensorMap mq_hi, const __grid_constant__ 
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
                  : "memory");
+  }
+}
+
+// A barrier expecting one arrival that never comes: the wait expires after
+// `spins` tries and the block records it, as the distance kernel does.
+__global__ void wait_timeout_kernel(uint32_t spins, int* err) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if (!mbar_wait(smem_u32(&bar), 0, spins)) atomicExch(err, 1);
   }
 }
 
@@ -385,17 +472,30 @@ int make_map(CUtensorMap* m, const float* p, int64_t rows, int dpad) {
   return IVFPQ_OK;
 }
 
-template <int KC>
+template <int KC, int MODE>
 int launch_tc(const CUtensorMap& qh, const CUtensorMap& ql, const CUtensorMap& xh,
               const CUtensorMap& xl, const TcArgs& args, int qtiles, cudaStream_t s) {
   // as many 32 KB stages as fit beside the resident query tile (224 KB total)
   constexpr int NSTAGE = (224 * 1024 - 2 * KC * kChunkBytes) / (2 * kChunkBytes);
-  auto kern = l2_tc_kernel<KC, NSTAGE>;
+  auto kern = l2_tc_kernel<KC, NSTAGE, MODE>;
   const size_t smem = TcSmem<KC, NSTAGE>::kTotal;
   IVFPQ_TRY(set_dynamic_smem(kern, smem));
-  kern<<<unsigned(qtiles * args.nsplit), 192, smem, s>>>(qh, ql, xh, xl, args);
-  IVFPQ_LAUNCHED_K(kern, smem, 192);
+  kern<<<unsigned(qtiles * args.nsplit), kTcThreads, smem, s>>>(qh, ql, xh, xl, args);
+  IVFPQ_LAUNCHED_K(kern, smem, kTcThreads);
   return IVFPQ_OK;
+}
+
+template <int MODE>
+int launch_mode(int kc, const CUtensorMap& qh, const CUtensorMap& ql, const CUtensorMap& xh,
+                const CUtensorMap& xl, const TcArgs& args, int qtiles, cudaStream_t s) {
+  switch (kc) {
+    case 1: return launch_tc<1, MODE>(qh, ql, xh, xl, args, qtiles, s);
+    case 2: return launch_tc<2, MODE>(qh, ql, xh, xl, args, qtiles, s);
+    case 3: return launch_tc<3, MODE>(qh, ql, xh, xl, args, qtiles, s);
+    case 4: return launch_tc<4, MODE>(qh, ql, xh, xl, args, qtiles, s);
+  }
+  set_error("tensor-core distances need d <= 128");
+  return IVFPQ_ERR_UNSUPPORTED;
 }
 
 }  // namespace
@@ -425,37 +525,91 @@ int l2_tc_prepare(const float* x, int64_t rows, int d, float* hi, float* lo, flo
   return IVFPQ_OK;
 }
 
-int l2_tc_tiles(const float* qhi, const float* qlo, const float* qnorm, int64_t nq,
-                const float* xhi, const float* xlo, const float* xnorm, int64_t n, int d,
-                float* D, int64_t ldd, int* err, cudaStream_t s) {
-  if (nq == 0 || n == 0) return IVFPQ_OK;
+namespace {
+// nsplit = 0: enough CTAs for several waves.
+int run_tc(const float* qhi, const float* qlo, int64_t nq, const float* xhi, const float* xlo,
+           int64_t n, int d, int mode, TcArgs& args, cudaStream_t s) {
   const int dpad = tc_dpad(d);
   CUtensorMap mqh, mql, mxh, mxl;
   IVFPQ_TRY(make_map(&mqh, qhi, nq, dpad));
   IVFPQ_TRY(make_map(&mql, qlo, nq, dpad));
   IVFPQ_TRY(make_map(&mxh, xhi, n, dpad));
   IVFPQ_TRY(make_map(&mxl, xlo, n, dpad));
-  TcArgs args;
+  args.nq = int(nq);
+  args.n = int(n);
+  args.ntiles_n = int(ceil_div(n, TN));
+  const int qtiles = int(ceil_div(nq, TM));
+  const int kc = dpad / TKC;
+  switch (mode) {
+    case kModeTile: return launch_mode<kModeTile>(kc, mqh, mql, mxh, mxl, args, qtiles, s);
+    case kModeGroupMin:
+      return launch_mode<kModeGroupMin>(kc, mqh, mql, mxh, mxl, args, qtiles, s);
+    default: return launch_mode<kModeFilter>(kc, mqh, mql, mxh, mxl, args, qtiles, s);
+  }
+}
+
+int default_split(int64_t nq, int64_t n) {
+  const int64_t qtiles = ceil_div(nq, TM), ntiles = ceil_div(n, TN);
+  return int(std::max<int64_t>(
+      1, std::min<int64_t>(ntiles, ceil_div(8 * int64_t(num_sms()), qtiles))));
+}
+}  // namespace
+
+int tc_filter_split(int64_t nq, int64_t n) { return default_split(nq, n); }
+
+int l2_tc_tiles(const float* qhi, const float* qlo, const float* qnorm, int64_t nq,
+                const float* xhi, const float* xlo, const float* xnorm, int64_t n, int d,
+                float* D, int64_t ldd, int* err, cudaStream_t s) {
+  if (nq == 0 || n == 0) return IVFPQ_OK;
+  TcArgs args{};
   args.qnorm = qnorm;
   args.xnorm = xnorm;
   args.D = D;
   args.ldd = ldd;
-  args.nq = int(nq);
-  args.n = int(n);
-  args.ntiles_n = int(ceil_div(n, TN));
   args.err = err;
-  const int qtiles = int(ceil_div(nq, TM));
-  // enough CTAs for several waves; each CTA covers a contiguous run of tiles
-  args.nsplit = int(std::max<int64_t>(
-      1, std::min<int64_t>(args.ntiles_n, ceil_div(8 * int64_t(num_sms()), qtiles))));
-  switch (dpad / TKC) {
-    case 1: return launch_tc<1>(mqh, mql, mxh, mxl, args, qtiles, s);
-    case 2: return launch_tc<2>(mqh, mql, mxh, mxl, args, qtiles, s);
-    case 3: return launch_tc<3>(mqh, mql, mxh, mxl, args, qtiles, s);
-    case 4: return launch_tc<4>(mqh, mql, mxh, mxl, args, qtiles, s);
-  }
-  set_error("tensor-core distances need d <= 128 (d = %d)", d);
-  return IVFPQ_ERR_UNSUPPORTED;
+  args.nsplit = default_split(nq, n);
+  return run_tc(qhi, qlo, nq, xhi, xlo, n, d, kModeTile, args, s);
+}
+
+int l2_tc_group_min(const float* qhi, const float* qlo, int64_t nq, const float* xhi,
+                    const float* xlo, const float* xnorm, int64_t n, int d, int nsplit,
+                    float* gmin, int* err, cudaStream_t s) {
+  if (nq == 0 || n == 0) return IVFPQ_OK;
+  TcArgs args{};
+  args.xnorm = xnorm;
+  args.err = err;
+  args.gmin = gmin;
+  args.nsplit = nsplit;
+  return run_tc(qhi, qlo, nq, xhi, xlo, n, d, kModeGroupMin, args, s);
+}
+
+int l2_tc_filter(const float* qhi, const float* qlo, const float* qnorm, int64_t nq,
+                 const float* xhi, const float* xlo, const float* xnorm, int64_t n, int d,
+                 const float* bound, int64_t bound_stride, int nsplit, uint64_t* cand, int* scnt,
+                 int cap_s, int* err, cudaStream_t s) {
+  if (nq == 0 || n == 0) return IVFPQ_OK;
+  TcArgs args{};
+  args.qnorm = qnorm;
+  args.xnorm = xnorm;
+  args.err = err;
+  args.bound = bound;
+  args.bound_stride = bound_stride;
+  args.nsplit = nsplit;
+  args.cand = cand;
+  args.scnt = scnt;
+  args.cap_s = cap_s;
+  return run_tc(qhi, qlo, nq, xhi, xlo, n, d, kModeFilter, args, s);
 }
 
 }  // namespace ivfpq
+
+extern "C" int ivfpq_selftest_wait_timeout(int spins, void* stream) {
+  using namespace ivfpq;
+  clear_error();
+  IVFPQ_REQUIRE(spins >= 1 && spins <= (1 << 20), "spins=%d outside [1, 2^20]", spins);
+  int* w = nullptr;
+  IVFPQ_TRY(device_status_word(&w));
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(uint32_t(spins), w);
+  IVFPQ_LAUNCHED();
+  return IVFPQ_OK;
+}

@@ -50,6 +50,10 @@ int kselect_device(const float* vals, int64_t rows, int64_t cols, int k, const S
 int l2_distance_tile(const float* Q, int64_t nq, const float* X, int64_t n, int d, float* D,
                      int64_t ldd, cudaStream_t s);
 
+// The current device's status word (abi_util.cu): kernels with bounded waits
+// set it when a wait expires; ivfpq_device_check reads and clears it.
+int device_status_word(int** out);
+
 // ---- tensor-core distance tiles (gemm_tc.cu) -------------------------------------
 // Operands for 3xTF32 distances: hi/lo split rows padded to tc_dpad(d) columns
 // and fp32 squared norms.
@@ -66,7 +70,32 @@ int l2_tc_prepare(const float* x, int64_t rows, int d, float* hi, float* lo, flo
 int l2_tc_tiles(const float* qhi, const float* qlo, const float* qnorm, int64_t nq,
                 const float* xhi, const float* xlo, const float* xnorm, int64_t n, int d,
                 float* D, int64_t ldd, int* err, cudaStream_t s);
+// u[i, j] = ||x_j||^2 - 2 <q_i, x_j> (= D[i, j] - ||q_i||^2, so each row is
+// ordered as D). Group-minimum pass over n columns with nsplit CTAs per
+// 128-row query tile: gmin[i * G + g] = min of u[i, j] over group g of the
+// columns, G = 128 * nsplit groups (column position mod 128 within each CTA's
+// contiguous run of column tiles); +inf for an empty group.
+int l2_tc_group_min(const float* qhi, const float* qlo, int64_t nq, const float* xhi,
+                    const float* xlo, const float* xnorm, int64_t n, int d, int nsplit,
+                    float* gmin, int* err, cudaStream_t s);
+// Filter pass: row i keeps the entries with u[i, j] <= bound[i * bound_stride]
+// (widened by a few ulps) as packed (order-preserving key of D << 32 | j) in
+// nseg = 2 * nsplit segments of cap_s entries:
+// cand[(i * nseg + seg) * cap_s ..], scnt[i * nseg + seg] = entries found (a
+// count above cap_s means entries were dropped).
+int l2_tc_filter(const float* qhi, const float* qlo, const float* qnorm, int64_t nq,
+                 const float* xhi, const float* xlo, const float* xnorm, int64_t n, int d,
+                 const float* bound, int64_t bound_stride, int nsplit, uint64_t* cand, int* scnt,
+                 int cap_s, int* err, cudaStream_t s);
+// CTAs per query tile that l2_tc_tiles would use for nq x n.
+int tc_filter_split(int64_t nq, int64_t n);
 
+// k-selection (k <= 256) over the candidate segments of l2_tc_filter; a row
+// with an overflowed segment is selected over exact distances between row i
+// of Q and all n rows of X instead (select_cand.cu).
+int select_candidates(const uint64_t* cand, const int* scnt, int nseg, int cap_s, int64_t rows,
+                      const float* Q, const float* X, int64_t n, int d, int k,
+                      const SelectOut& out, cudaStream_t s);
 // ---- flat / coarse search on distance tiles (flat.cu) ----------------------------
 // k nearest rows of X for each row of Q under squared L2; output as SelectOut
 // (Float with column ids, or Probes).

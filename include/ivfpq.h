@@ -221,6 +221,22 @@ int kselect(const float* vals, int64_t rows, int64_t cols, int k, float* out_val
 int kselect_noalloc(const float* vals, int64_t rows, int64_t cols, int k, float* out_vals,
                     int64_t* out_idx, void* stream);
 
+/* ivfpq_device_check -- synchronises `stream` and reports whether any kernel
+ * of this library on the current device gave up a bounded wait since the
+ * last check (the tensor-core distance pipeline waits on its own copies and
+ * MMAs with an iteration limit; on expiry it stops, releases its resources
+ * and sets a per-device status word instead of hanging). Clears the word.
+ * Returns IVFPQ_OK, or IVFPQ_ERR_TIMEOUT (the results of the calls since the
+ * previous check are then invalid), or IVFPQ_ERR_CUDA. */
+int ivfpq_device_check(void* stream);
+
+/* ivfpq_selftest_wait_timeout -- launches one block that waits, with an
+ * iteration limit of `spins`, on a barrier phase that nothing completes, the
+ * same bounded wait the distance pipeline uses; the block records the expiry
+ * in the status word and returns. A host-visible check of that mechanism:
+ * ivfpq_device_check then returns IVFPQ_ERR_TIMEOUT. spins: 1 .. 2^20. */
+int ivfpq_selftest_wait_timeout(int spins, void* stream);
+
 /* ivfpq_last_error -- message for the most recent failure on this thread
  * (empty string if none). The pointer stays valid until the next call into
  * the library from this thread. */
