@@ -42,6 +42,7 @@ SIGNATURES = {
     "ivfpq_search_preassigned": (_I, [_VP, _VP, _I64, _I, _VP, _I, _VP, _VP, _VP]),
     "ivfpq_set_profiling": (_I, [_VP, _I]),
     "ivfpq_stage_times": (_I, [_VP, C.POINTER(C.c_float), C.POINTER(C.c_int)]),
+    "ivfpq_last_scan_kernel": (C.c_char_p, [_VP]),
     "ivfpq_kernel_launches": (C.c_uint64, []),
     "flat_knn": (_I, [_VP, _I64, _I, _VP, _I64, _I, _VP, _VP, _VP]),
     "kselect": (_I, [_VP, _I64, _I64, _I, _VP, _VP, _VP]),
@@ -238,6 +239,12 @@ def ivfpq_stage_times(index):
     n = C.c_int(0)
     _check("ivfpq_stage_times", lib().ivfpq_stage_times(index.handle, buf, C.byref(n)))
     return list(buf), n.value
+
+
+def last_scan_kernel(index):
+    """Name of the list-scan kernel family the index's last search used."""
+    r = lib().ivfpq_last_scan_kernel(index.handle)
+    return r.decode() if r else None
 
 
 def kernel_launches():

@@ -28,6 +28,7 @@ struct SelectOut {
   const int64_t* id_map = nullptr;  // Dist: slot -> id
   uint32_t* pkeys = nullptr;      // Partial: [rows][chunks][k]
   uint32_t* pidx = nullptr;
+  const int* row_mask = nullptr;  // if set, rows with row_mask[row] == 0 are skipped
 };
 
 // Rows of fp32 values: row r holds vals[r*cols .. r*cols+cols). The columns of
@@ -108,6 +109,7 @@ int knn_by_tiles(const float* Q, int64_t nq, const float* X, int64_t n, int d, i
 // ---- the index -------------------------------------------------------------------------
 struct ivfpq_index {
   int d = 0, nlist = 0, m = 0, nbits = 8, dsub = 0, dsub4 = 0;
+  std::atomic<const char*> last_scan_kernel{nullptr};  // static name, for reports
   int lut_type = IVFPQ_LUT_FP32;
   int device = 0;
   float* centroids = nullptr;   // [nlist, d]

@@ -30,11 +30,9 @@ IVFPQ_EXTERN_SCAN(16, 64)
 IVFPQ_EXTERN_SCAN(16, 128)
 IVFPQ_EXTERN_SCAN(16, 256)
 
-#define IVFPQ_EXTERN_SCAN2(MW, DS)                                                                 \
-  extern template int launch_scan2<MW, DS, 32>(const ScanParams&, int64_t, cudaStream_t);         \
-  extern template int launch_scan2<MW, DS, 64>(const ScanParams&, int64_t, cudaStream_t);         \
-  extern template int launch_scan2<MW, DS, 128>(const ScanParams&, int64_t, cudaStream_t);        \
-  extern template int launch_scan2<MW, DS, 256>(const ScanParams&, int64_t, cudaStream_t);
+#define IVFPQ_EXTERN_SCAN2(MW, DS)                                                         \
+  extern template int launch_scan2<MW, DS, 32>(const ScanParams&, int64_t, cudaStream_t); \
+  extern template int launch_scan2<MW, DS, 64>(const ScanParams&, int64_t, cudaStream_t);
 IVFPQ_EXTERN_SCAN2(8, 3)
 IVFPQ_EXTERN_SCAN2(8, 4)
 IVFPQ_EXTERN_SCAN2(4, 8)
@@ -42,22 +40,28 @@ IVFPQ_EXTERN_SCAN2(4, 4)
 IVFPQ_EXTERN_SCAN2(2, 12)
 IVFPQ_EXTERN_SCAN2(2, 8)
 
-// The register-codebook kernel (scan2.cuh) for fp32 tables, k <= 256 and the
-// (m, d/m) shapes it is built for; 1 = launched, 0 = not applicable.
-template <int K>
-int try_scan2_k(const ScanParams& p, int64_t nq, cudaStream_t s, int* launched) {
+// The register-codebook kernel (scan2.cuh) with KW-entry warp queues, for
+// the (m, d/m) shapes it is built for; 1 = launched, 0 = not applicable.
+template <int KW>
+int try_scan2_kw(const ScanParams& p, int64_t nq, cudaStream_t s, int* launched) {
   *launched = 1;
   const int key = p.m * 100 + p.dsub;
   switch (key) {
-    case 3203: return launch_scan2<8, 3, K>(p, nq, s);
-    case 3204: return launch_scan2<8, 4, K>(p, nq, s);
-    case 1608: return launch_scan2<4, 8, K>(p, nq, s);
-    case 1604: return launch_scan2<4, 4, K>(p, nq, s);
-    case 812: return launch_scan2<2, 12, K>(p, nq, s);
-    case 808: return launch_scan2<2, 8, K>(p, nq, s);
+    case 3203: return launch_scan2<8, 3, KW>(p, nq, s);
+    case 3204: return launch_scan2<8, 4, KW>(p, nq, s);
+    case 1608: return launch_scan2<4, 8, KW>(p, nq, s);
+    case 1604: return launch_scan2<4, 4, KW>(p, nq, s);
+    case 812: return launch_scan2<2, 12, KW>(p, nq, s);
+    case 808: return launch_scan2<2, 8, KW>(p, nq, s);
   }
   *launched = 0;
   return IVFPQ_OK;
+}
+
+bool scan2_shape(const ScanParams& p) {
+  const int key = p.m * 100 + p.dsub;
+  return p.lut_type == IVFPQ_LUT_FP32 && p.m * p.dsub == p.d && p.k <= 256 &&
+         (key == 3203 || key == 3204 || key == 1608 || key == 1604 || key == 812 || key == 808);
 }
 
 // Code words per vector as a template argument where a specialised kernel
@@ -83,17 +87,8 @@ int queue_len(int k) {
   return K;
 }
 
-int launch_scan(const ScanParams& p, int64_t nq, cudaStream_t s) {
-  if (p.lut_type == IVFPQ_LUT_FP32 && p.m * p.dsub == p.d) {
-    int launched = 0, st = IVFPQ_OK;
-    switch (queue_len(p.k)) {
-      case 32: st = try_scan2_k<32>(p, nq, s, &launched); break;
-      case 64: st = try_scan2_k<64>(p, nq, s, &launched); break;
-      case 128: st = try_scan2_k<128>(p, nq, s, &launched); break;
-      case 256: st = try_scan2_k<256>(p, nq, s, &launched); break;
-    }
-    if (launched || st != IVFPQ_OK) return st;
-  }
+// The general kernel (scan.cuh): BlockSelect with K-entry queues.
+int launch_scan_general(const ScanParams& p, int64_t nq, cudaStream_t s) {
   switch (queue_len(p.k)) {
     case 32: return launch_scan_k<32>(p, nq, s);
     case 64: return launch_scan_k<64>(p, nq, s);
@@ -105,6 +100,23 @@ int launch_scan(const ScanParams& p, int64_t nq, cudaStream_t s) {
   }
   set_error("k=%d above %d", p.k, IVFPQ_MAX_K);
   return IVFPQ_ERR_INVALID_ARG;
+}
+
+// Queries whose result may have lost an entry to a short warp queue: some
+// full queue (last key real) whose last key is not above the merged k-th
+// key. kth: merged distances [nq, k] (row's k-th at kth[q * k + k - 1]).
+__global__ void warp_queue_check_kernel(const uint32_t* __restrict__ pkeys, int64_t nq,
+                                        int groups, int kw, const float* __restrict__ kth,
+                                        int k, int* __restrict__ flags) {
+  const int64_t q = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (q >= nq) return;
+  const uint32_t theta = __float_as_uint(kth[q * k + k - 1]);
+  int f = 0;
+  for (int g = 0; g < groups; ++g) {
+    const uint32_t last = pkeys[(q * groups + g) * kw + kw - 1];
+    f |= last != kSentinelKey && last <= theta;
+  }
+  flags[q] = f;
 }
 
 const size_t kMaxEventSets = 4096;
@@ -171,19 +183,58 @@ int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int npro
   p.lut_type = ix->lut_type;
   plan_chunks(nq, nprobe, &p.per_chunk, &p.nchunks);
   Workspace ws(s);
-  const size_t np = size_t(nq) * p.nchunks * k;
-  IVFPQ_TRY(ws.alloc(&p.pkeys, np));
-  IVFPQ_TRY(ws.alloc(&p.pidx, np));
-  record(ix, 2, s);
-  IVFPQ_TRY(launch_scan(p, nq, s));
-  record(ix, 3, s);
   SelectOut o;
   o.kind = OutKind::Dist;
   o.vals = out_dist;
   o.idx64 = out_ids;
   o.id_map = ix->ids;
-  const int64_t len = int64_t(p.nchunks) * k;
+  auto* mix = const_cast<ivfpq_index*>(ix);
+  if (!scan2_shape(p)) {
+    const size_t np = size_t(nq) * p.nchunks * k;
+    IVFPQ_TRY(ws.alloc(&p.pkeys, np));
+    IVFPQ_TRY(ws.alloc(&p.pidx, np));
+    record(ix, 2, s);
+    IVFPQ_TRY(launch_scan_general(p, nq, s));
+    mix->last_scan_kernel.store("ivfpq_scan_kernel");
+    record(ix, 3, s);
+    const int64_t len = int64_t(p.nchunks) * k;
+    IVFPQ_TRY(select_pairs(p.pkeys, p.pidx, nq, len, k, 1, len, o, s));
+    record(ix, 4, s);
+    return IVFPQ_OK;
+  }
+  // register-codebook kernel: per-warp queues of kw entries, unmerged
+  const int kw = scan2_kw(k);
+  const int groups = p.nchunks * kScan2Warps;
+  const size_t np = size_t(nq) * groups * kw;
+  IVFPQ_TRY(ws.alloc(&p.pkeys, np));
+  IVFPQ_TRY(ws.alloc(&p.pidx, np));
+  record(ix, 2, s);
+  int launched = 0;
+  if (kw == 32) IVFPQ_TRY(try_scan2_kw<32>(p, nq, s, &launched));
+  else IVFPQ_TRY(try_scan2_kw<64>(p, nq, s, &launched));
+  IVFPQ_REQUIRE(launched, "scan: no register-codebook kernel for m=%d d/m=%d", p.m, p.dsub);
+  mix->last_scan_kernel.store("ivfpq_scan2_kernel");
+  record(ix, 3, s);
+  const int64_t len = int64_t(groups) * kw;
   IVFPQ_TRY(select_pairs(p.pkeys, p.pidx, nq, len, k, 1, len, o, s));
+  if (kw < k) {
+    // repair the queries whose merged result a short queue may have cut
+    int* flags = nullptr;
+    IVFPQ_TRY(ws.alloc(&flags, size_t(nq)));
+    warp_queue_check_kernel<<<unsigned(ceil_div(nq, 256)), 256, 0, s>>>(p.pkeys, nq, groups, kw,
+                                                                       out_dist, k, flags);
+    IVFPQ_LAUNCHED();
+    ScanParams r = p;
+    r.qmask = flags;
+    const size_t nr = size_t(nq) * p.nchunks * k;
+    IVFPQ_TRY(ws.alloc(&r.pkeys, nr));
+    IVFPQ_TRY(ws.alloc(&r.pidx, nr));
+    IVFPQ_TRY(launch_scan_general(r, nq, s));
+    SelectOut ro = o;
+    ro.row_mask = flags;
+    const int64_t rlen = int64_t(p.nchunks) * k;
+    IVFPQ_TRY(select_pairs(r.pkeys, r.pidx, nq, rlen, k, 1, rlen, ro, s));
+  }
   record(ix, 4, s);
   return IVFPQ_OK;
 }
@@ -264,6 +315,10 @@ extern "C" int ivfpq_set_profiling(ivfpq_index* ix, int enable) {
   ix->ev_used = 0;
   ix->cur_set = -1;
   return IVFPQ_OK;
+}
+
+extern "C" const char* ivfpq_last_scan_kernel(const ivfpq_index* ix) {
+  return ix ? ix->last_scan_kernel.load() : nullptr;
 }
 
 extern "C" int ivfpq_stage_times(const ivfpq_index* ix, float* ms, int* nsearches) {

@@ -45,10 +45,11 @@ struct ScanParams {
   const int32_t* list_len;   // [nlist]
   const int64_t* list_block_off;  // [nlist + 1]
   const uint8_t* codes;      // blocks of 32 * m bytes
-  uint32_t* pkeys;           // [nq, nchunks, k]
+  uint32_t* pkeys;           // [nq, nchunks, k] (scan2: [nq, nchunks, warps, kw])
   uint32_t* pidx;
   int d, m, dsub, dsub4, nlist, nprobe, per_chunk, nchunks, k;
   int lut_type;              // IVFPQ_LUT_FP32 / FP16 / FP8
+  const int* qmask = nullptr;  // if set, only queries q with qmask[q] != 0 are scanned
 };
 
 constexpr int kScanWarps = 8;
@@ -331,6 +332,7 @@ ivfpq_scan_kernel(const ScanParams p) {
 
   const int64_t q = int64_t(blockIdx.x) / p.nchunks;
   const int chunk = int(int64_t(blockIdx.x) % p.nchunks);
+  if (p.qmask && !p.qmask[q]) return;  // the same for the whole block
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   WarpSelect<K, T> ws;
   ws.init(lane);

@@ -11,9 +11,16 @@
 //    (warp w, lane i) owns sub-quantizer jj = i mod GS of the group and the
 //    reproduction values e = (s*16 + w) * QQ + i / GS, QQ = 32 / GS;
 //  * the table of list i+1 is built into one buffer while list i is scanned
-//    with the other, so each probed list costs one block barrier.
-// The shared-memory table layout, the rotated code layout, the look-up
-// addressing and the selection are those of scan.cuh.
+//    with the other, so each probed list costs one block barrier;
+//  * each warp keeps only its own KW best (WarpSelect with a KW-entry warp
+//    queue, KW < k allowed) and writes them out unmerged; the cross-chunk
+//    merge selects the k best of all warps' entries. That is exact unless a
+//    warp's k-th-best contribution was cut off by its short queue, which the
+//    merge detects (a full warp queue whose last key is not above the merged
+//    k-th key) and repairs by scanning that query again with full-length
+//    queues (ivfpq_search.cu).
+// The shared-memory table layout, the rotated code layout and the look-up
+// addressing are those of scan.cuh.
 #pragma once
 
 #include "scan.cuh"
@@ -34,11 +41,11 @@ struct Scan2Shape {
   static constexpr int DS4 = (DS + 3) & ~3;
 };
 
-template <int MW, int DS, int K>
+template <int MW, int DS, int KW>
 __global__ void __launch_bounds__(kScan2Warps * 32, 1)
 ivfpq_scan2_kernel(const ScanParams p) {
   using Sh = Scan2Shape<MW, DS>;
-  constexpr int T = ThreadQ<K>::value;
+  constexpr int T = ThreadQ<KW>::value;
   constexpr int NW = kScan2Warps;
   constexpr int m = Sh::M;
   extern __shared__ __align__(16) uint32_t scan2_smem[];
@@ -47,6 +54,7 @@ ivfpq_scan2_kernel(const ScanParams p) {
 
   const int64_t q = int64_t(blockIdx.x) / p.nchunks;
   const int chunk = int(int64_t(blockIdx.x) % p.nchunks);
+  if (p.qmask && !p.qmask[q]) return;  // the same for the whole block
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int jj = lane & (Sh::GS - 1), qq = lane >> Sh::LOG_GS;
 
@@ -86,7 +94,7 @@ ivfpq_scan2_kernel(const ScanParams p) {
     }
   };
 
-  WarpSelect<K, T> ws;
+  WarpSelect<KW, T> ws;
   ws.init(lane);
   const int p0 = chunk * p.per_chunk;
   const int p1 = min(p.nprobe, p0 + p.per_chunk);
@@ -129,30 +137,25 @@ ivfpq_scan2_kernel(const ScanParams p) {
     __syncthreads();  // cur may be overwritten next; nxt is complete
   }
   ws.finalize();
-  block_merge<K, T, NW>(ws, scan2_smem, scan2_smem + NW * K, warp);
-  if (warp == 0) {
-    const int64_t o = (q * p.nchunks + chunk) * p.k;
+  // this warp's KW best, ascending (sentinel-padded)
+  const int64_t o = ((q * p.nchunks + chunk) * NW + warp) * KW;
 #pragma unroll
-    for (int r = 0; r < K / 32; ++r) {
-      const int i = 32 * r + lane;
-      if (i < p.k) {
-        p.pkeys[o + i] = ws.wk[r];
-        p.pidx[o + i] = ws.wv[r];
-      }
-    }
+  for (int r = 0; r < KW / 32; ++r) {
+    p.pkeys[o + 32 * r + lane] = ws.wk[r];
+    p.pidx[o + 32 * r + lane] = ws.wv[r];
   }
 }
 
-inline size_t scan2_smem_bytes(int K) {
-  const size_t luts = size_t(2) * kGroupWords * 4;
-  const size_t merge = size_t(kScan2Warps) * K * 8;
-  return luts > merge ? luts : merge;
-}
+inline size_t scan2_smem_bytes() { return size_t(2) * kGroupWords * 4; }
 
-template <int MW, int DS, int K>
+// Warp-queue length for a result of k <= 256: each warp's share of the k
+// best is about k / 16, so 32 entries (64 for k > 128) leave a wide margin.
+inline int scan2_kw(int k) { return k <= 128 ? 32 : 64; }
+
+template <int MW, int DS, int KW>
 int launch_scan2(const ScanParams& p, int64_t nq, cudaStream_t s) {
-  auto kern = ivfpq_scan2_kernel<MW, DS, K>;
-  const size_t smem = scan2_smem_bytes(K);
+  auto kern = ivfpq_scan2_kernel<MW, DS, KW>;
+  const size_t smem = scan2_smem_bytes();
   IVFPQ_TRY(set_dynamic_smem(kern, smem));
   const int64_t blocks = nq * p.nchunks;
   kern<<<unsigned(blocks), kScan2Warps * 32, smem, s>>>(p);
@@ -162,5 +165,5 @@ int launch_scan2(const ScanParams& p, int64_t nq, cudaStream_t s) {
 
 }  // namespace ivfpq
 
-#define IVFPQ_INST_SCAN2(MW, DS, K) \
-  template int ivfpq::launch_scan2<MW, DS, K>(const ivfpq::ScanParams&, int64_t, cudaStream_t);
+#define IVFPQ_INST_SCAN2(MW, DS, KW) \
+  template int ivfpq::launch_scan2<MW, DS, KW>(const ivfpq::ScanParams&, int64_t, cudaStream_t);

@@ -3,9 +3,5 @@
 
 IVFPQ_INST_SCAN2(4, 8, 32)
 IVFPQ_INST_SCAN2(4, 8, 64)
-IVFPQ_INST_SCAN2(4, 8, 128)
-IVFPQ_INST_SCAN2(4, 8, 256)
 IVFPQ_INST_SCAN2(4, 4, 32)
 IVFPQ_INST_SCAN2(4, 4, 64)
-IVFPQ_INST_SCAN2(4, 4, 128)
-IVFPQ_INST_SCAN2(4, 4, 256)

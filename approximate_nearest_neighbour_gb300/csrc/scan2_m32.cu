@@ -3,9 +3,5 @@
 
 IVFPQ_INST_SCAN2(8, 3, 32)
 IVFPQ_INST_SCAN2(8, 3, 64)
-IVFPQ_INST_SCAN2(8, 3, 128)
-IVFPQ_INST_SCAN2(8, 3, 256)
 IVFPQ_INST_SCAN2(8, 4, 32)
 IVFPQ_INST_SCAN2(8, 4, 64)
-IVFPQ_INST_SCAN2(8, 4, 128)
-IVFPQ_INST_SCAN2(8, 4, 256)

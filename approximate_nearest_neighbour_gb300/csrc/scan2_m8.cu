@@ -3,9 +3,5 @@
 
 IVFPQ_INST_SCAN2(2, 12, 32)
 IVFPQ_INST_SCAN2(2, 12, 64)
-IVFPQ_INST_SCAN2(2, 12, 128)
-IVFPQ_INST_SCAN2(2, 12, 256)
 IVFPQ_INST_SCAN2(2, 8, 32)
 IVFPQ_INST_SCAN2(2, 8, 64)
-IVFPQ_INST_SCAN2(2, 8, 128)
-IVFPQ_INST_SCAN2(2, 8, 256)

@@ -53,6 +53,7 @@ select_rows_kernel(const float* __restrict__ vals, int64_t cols, int64_t chunk_l
   extern __shared__ uint32_t sm_sel[];
   const int64_t row = blockIdx.x;
   const int64_t chunk = blockIdx.y;
+  if (out.o.row_mask && !out.o.row_mask[row]) return;  // the same for the whole block
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WarpSelect<K, T> ws;
   ws.init(lane);
@@ -106,6 +107,7 @@ select_pairs_kernel(const uint32_t* __restrict__ keys, const uint32_t* __restric
   extern __shared__ uint32_t sm_sel[];
   const int64_t row = blockIdx.x;
   const int64_t chunk = blockIdx.y;
+  if (out.o.row_mask && !out.o.row_mask[row]) return;  // the same for the whole block
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   WarpSelect<K, T> ws;
   ws.init(lane);

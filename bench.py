@@ -36,8 +36,9 @@ sys.path.insert(0, ROOT)
 from approximate_nearest_neighbour_gb300 import synthetic as S  # noqa: E402
 
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_FILE = os.path.join(ROOT, "profiles", "ivfpq_scan_large.md")
-SCAN_SOURCES = ["scan.cuh", "select.cuh", "layout.cuh", "common.cuh"]
+# ncu summary of the scan kernel on the large workload, per kernel family
+PROFILE_FILE = os.path.join(ROOT, "profiles", "{kernel}_large.md")
+SCAN_SOURCES = ["scan2.cuh", "scan.cuh", "select.cuh", "layout.cuh", "common.cuh"]
 
 
 def parse():
@@ -82,13 +83,14 @@ def scan_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
+def profiled_traffic(kernel):
     """DRAM bytes per scan launch from the committed ncu summary, if it was
     taken on the current scan source; else None."""
-    if not os.path.exists(PROFILE_FILE):
+    path = PROFILE_FILE.format(kernel=kernel)
+    if not os.path.exists(path):
         return None
     vals = {}
-    with open(PROFILE_FILE) as f:
+    with open(path) as f:
         for line in f:
             if ":" in line and line.strip().startswith("- "):
                 k, v = line.strip()[2:].split(":", 1)
@@ -270,6 +272,7 @@ def run_ours(args):
         dist.barrier()
     clk = clocks.stop()
     launches = B.kernel_launches() - launches0
+    scan_kernel = B.last_scan_kernel(ix)
     elapsed = ev0.elapsed_time(ev1) / 1e3
     sums, count = B.ivfpq_stage_times(ix)
     B.ivfpq_set_profiling(ix, False)
@@ -311,7 +314,7 @@ def run_ours(args):
         peak, peak_kind = peaks()
         scan_ms = sums[2] / max(count, 1)
         achieved = scan_bytes / (scan_ms / 1e3) / 1e9
-        traffic = profiled_traffic()
+        traffic = profiled_traffic(scan_kernel)
         if traffic is not None and (args.n is not None or args.nlist is not None):
             traffic = None
         total_q = nq * world * args.steps
@@ -322,7 +325,7 @@ def run_ours(args):
             "ms_per_step": 1e3 * elapsed / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": config_dict(args, data),
-            "roofline": {"bound": "hbm", "kernel": "ivfpq_scan_kernel", "achieved": achieved,
+            "roofline": {"bound": "hbm", "kernel": scan_kernel, "achieved": achieved,
                          "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "peak_source": f"{peak_kind} hbm_gbs (copy)",
                          "traffic": traffic, "algorithmic_bytes_per_launch": scan_bytes,

@@ -170,6 +170,12 @@ int ivfpq_search_preassigned(const ivfpq_index* index, const float* queries, int
 int ivfpq_set_profiling(ivfpq_index* index, int enable);
 int ivfpq_stage_times(const ivfpq_index* index, float* ms, int* nsearches);
 
+/* ivfpq_last_scan_kernel -- name of the list-scan kernel family that the
+ * most recent search of this index launched ("ivfpq_scan2_kernel": codebook
+ * in registers, double-buffered fp32 tables; "ivfpq_scan_kernel": the general
+ * kernel), or NULL before the first search; a measurement aid. */
+const char* ivfpq_last_scan_kernel(const ivfpq_index* index);
+
 /* ivfpq_kernel_launches -- number of CUDA kernels this library has launched
  * since it was loaded (all threads); a measurement aid. */
 uint64_t ivfpq_kernel_launches(void);

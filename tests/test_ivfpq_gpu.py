@@ -161,6 +161,42 @@ def test_preassigned_probes_with_repeats(B):
     assert np.all(np.abs(g - od) <= tol(od))
 
 
+@pytest.mark.parametrize("k,blocks", [(100, (0, 16, 32)), (200, (0, 16, 32, 48)), (40, (16, 48))])
+def test_results_concentrated_in_one_warp_are_repaired(B, k, blocks):
+    """The list scan's per-warp queues are shorter than k (each warp of the
+    register-codebook kernel takes code blocks b = w mod 16 of every list).
+    Here the best vectors of the one probed list all sit in blocks that one
+    warp scans, more of them than its queue holds: the merge must detect it
+    and the query must be scanned again with full-length queues."""
+    import torch
+    rng = np.random.default_rng(k)
+    nlist, m, dsub, n = 4, 32, 3, 4096
+    d = m * dsub
+    cent = rng.standard_normal((nlist, d)).astype(np.float32)
+    cb = (0.3 * rng.standard_normal((m, 256, dsub))).astype(np.float32)
+    q = (cent[[0, 0, 1]] + 0.2 * rng.standard_normal((3, d))).astype(np.float32)
+    T = oracle.lut(q[0].astype(np.float64) - cent[0], cb)
+    order = np.argsort(T, axis=1)
+    codes = rng.integers(0, 256, (n, m)).astype(np.uint8)
+    for b in blocks:
+        for i in range(32 * b, 32 * b + 32):
+            c = order[:, 0].copy()
+            j = rng.integers(0, m)
+            c[j] = order[j, rng.integers(1, 4)]
+            codes[i] = c
+    list_ids = np.zeros(n, np.int32)
+    list_ids[-100:] = 1
+    ids = np.arange(n, dtype=np.int64) * 7 + 3
+    ix = make_index(B, cent, cb, codes, list_ids, ids)
+    probes = np.array([[0], [0], [1]], np.int32)
+    gd, gi = B.ivfpq_search_preassigned(ix, _t(q), _t(probes), k)
+    torch.cuda.synchronize()
+    off, codes_l, ids_l = oracle.to_lists(codes, list_ids, ids, nlist)
+    od, oi, _ = oracle.ivfpq_search(q, cent, cb, off, codes_l, ids_l, 1, k + 64,
+                                    forced_probes=probes)
+    compare_knn(gd.cpu().numpy(), gi.cpu().numpy(), od, oi, context="warp repair")
+
+
 def test_all_lists_on_exactly_encoded_set_matches_flat(B):
     """Vectors built as centroid + codewords: IVF-PQ with nprobe = nlist and
     flat k-NN on the decoded vectors agree (two different GPU paths)."""
