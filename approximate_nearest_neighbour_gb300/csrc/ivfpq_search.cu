@@ -202,7 +202,12 @@ int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int npro
     record(ix, 4, s);
     return IVFPQ_OK;
   }
-  // register-codebook kernel: per-warp queues of kw entries, unmerged
+  // register-codebook kernel: per-warp queues of kw entries, unmerged; at
+  // most kScan2MaxLists lists per block
+  if (p.per_chunk > kScan2MaxLists) {
+    p.per_chunk = kScan2MaxLists;
+    p.nchunks = int(ceil_div(nprobe, kScan2MaxLists));
+  }
   const int kw = scan2_kw(k);
   const int groups = p.nchunks * kScan2Warps;
   const size_t np = size_t(nq) * groups * kw;

@@ -12,6 +12,10 @@
 //    reproduction values e = (s*16 + w) * QQ + i / GS, QQ = 32 / GS;
 //  * the table of list i+1 is built into one buffer while list i is scanned
 //    with the other, so each probed list costs one block barrier;
+//  * the block's probe list (list id, length, first block) is staged in
+//    shared memory once, and each warp loads its first code block of list
+//    i+1 before the barrier that ends list i, so no list starts with a chain
+//    of dependent global loads;
 //  * each warp keeps only its own KW best (WarpSelect with a KW-entry warp
 //    queue, KW < k allowed) and writes them out unmerged; the cross-chunk
 //    merge selects the k best of all warps' entries. That is exact unless a
@@ -28,6 +32,7 @@
 namespace ivfpq {
 
 constexpr int kScan2Warps = 16;
+constexpr int kScan2MaxLists = 256;  // probed lists per block (per query chunk)
 
 template <int MW, int DS>
 struct Scan2Shape {
@@ -97,43 +102,56 @@ ivfpq_scan2_kernel(const ScanParams p) {
   WarpSelect<KW, T> ws;
   ws.init(lane);
   const int p0 = chunk * p.per_chunk;
-  const int p1 = min(p.nprobe, p0 + p.per_chunk);
-  const int32_t* qprobes = p.probes + q * p.nprobe;
+  const int n = max(0, min(p.nprobe, p0 + p.per_chunk) - p0);  // <= kScan2MaxLists
   const uint32_t lane4 = uint32_t(lane) * 4;
-  auto valid_list = [&](int l) { return l >= 0 && l < p.nlist; };
 
-  if (tid == 0 && p0 < p1) prefetch_list(p, qprobes[p0], m);
-  if (p0 < p1 && valid_list(qprobes[p0])) build(qprobes[p0], buf0);
+  // the block's lists: id (-1 if out of range), length, first block
+  int* s_list = reinterpret_cast<int*>(scan2_smem + 2 * kGroupWords);
+  int* s_len = s_list + kScan2MaxLists;
+  int64_t* s_boff = reinterpret_cast<int64_t*>(s_len + kScan2MaxLists);
+  for (int i = tid; i < n; i += NW * 32) {
+    const int l = p.probes[q * p.nprobe + p0 + i];
+    const bool v = l >= 0 && l < p.nlist;
+    s_list[i] = v ? l : -1;
+    s_len[i] = v ? p.list_len[l] : 0;
+    s_boff[i] = v ? p.list_block_off[l] : 0;
+  }
   __syncthreads();
 
-  for (int pi = p0; pi < p1; ++pi) {
-    const int l = qprobes[pi];
-    float* cur = ((pi - p0) & 1) ? buf1 : buf0;
-    float* nxt = ((pi - p0) & 1) ? buf0 : buf1;
-    if (pi + 1 < p1) {
-      const int ln = qprobes[pi + 1];
-      if (tid == 0) prefetch_list(p, ln, m);
-      if (valid_list(ln)) build(ln, nxt);
+  if (tid == 0) {
+    if (n > 0 && s_list[0] >= 0) prefetch_list(p, s_list[0], m);
+    if (n > 1 && s_list[1] >= 0) prefetch_list(p, s_list[1], m);
+  }
+  if (n > 0 && s_list[0] >= 0) build(s_list[0], buf0);
+  uint32_t c0[MW], c1[MW];
+  if (n > 0 && warp < (s_len[0] + 31) >> 5)
+    load_codes<MW>(p.codes + (s_boff[0] + warp) * 32 * m, lane, c0);
+  __syncthreads();
+
+  for (int i = 0; i < n; ++i) {
+    float* cur = (i & 1) ? buf1 : buf0;
+    float* nxt = (i & 1) ? buf0 : buf1;
+    if (i + 1 < n) {
+      if (tid == 0 && i + 2 < n && s_list[i + 2] >= 0) prefetch_list(p, s_list[i + 2], m);
+      if (s_list[i + 1] >= 0) build(s_list[i + 1], nxt);
     }
-    if (valid_list(l)) {
-      const int len = p.list_len[l];
-      const int64_t boff = p.list_block_off[l];
-      const int nb = (len + 31) >> 5;
-      const uint8_t* lcodes = p.codes + boff * 32 * m;
-      const char* lut_bytes = reinterpret_cast<const char*>(cur);
-      uint32_t c0[MW], c1[MW];
-      int b = warp;
-      if (b < nb) load_codes<MW>(lcodes + int64_t(b) * 32 * m, lane, c0);
-      for (; b < nb; b += NW) {
-        const int bn = b + NW;
-        if (bn < nb) load_codes<MW>(lcodes + int64_t(bn) * 32 * m, lane, c1);
-        const float dist = adc_sum<MW, IVFPQ_LUT_FP32>(c0, lut_bytes, lane4);
-        const bool valid = b * 32 + lane < len;
-        ws.add(valid ? __float_as_uint(dist) : kSentinelKey, uint32_t((boff + b) * 32 + lane));
+    const int len = s_len[i];
+    const int64_t boff = s_boff[i];
+    const int nb = (len + 31) >> 5;
+    const uint8_t* lcodes = p.codes + boff * 32 * m;
+    const char* lut_bytes = reinterpret_cast<const char*>(cur);
+    for (int b = warp; b < nb; b += NW) {
+      const int bn = b + NW;
+      if (bn < nb) load_codes<MW>(lcodes + int64_t(bn) * 32 * m, lane, c1);
+      const float dist = adc_sum<MW, IVFPQ_LUT_FP32>(c0, lut_bytes, lane4);
+      const bool valid = b * 32 + lane < len;
+      ws.add(valid ? __float_as_uint(dist) : kSentinelKey, uint32_t((boff + b) * 32 + lane));
 #pragma unroll
-        for (int w = 0; w < MW; ++w) c0[w] = c1[w];
-      }
+      for (int w = 0; w < MW; ++w) c0[w] = c1[w];
     }
+    // this warp's first block of the next list, before the barrier
+    if (i + 1 < n && warp < (s_len[i + 1] + 31) >> 5)
+      load_codes<MW>(p.codes + (s_boff[i + 1] + warp) * 32 * m, lane, c0);
     __syncthreads();  // cur may be overwritten next; nxt is complete
   }
   ws.finalize();
@@ -146,7 +164,8 @@ ivfpq_scan2_kernel(const ScanParams p) {
   }
 }
 
-inline size_t scan2_smem_bytes() { return size_t(2) * kGroupWords * 4; }
+// two table buffers and the staged probe list
+inline size_t scan2_smem_bytes() { return size_t(2) * kGroupWords * 4 + kScan2MaxLists * 16; }
 
 // Warp-queue length for a result of k <= 256: each warp's share of the k
 // best is about k / 16, so 32 entries (64 for k > 128) leave a wide margin.
