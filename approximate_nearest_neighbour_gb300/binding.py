@@ -47,6 +47,7 @@ SIGNATURES = {
     "flat_knn": (_I, [_VP, _I64, _I, _VP, _I64, _I, _VP, _VP, _VP]),
     "kselect": (_I, [_VP, _I64, _I64, _I, _VP, _VP, _VP]),
     "kselect_noalloc": (_I, [_VP, _I64, _I64, _I, _VP, _VP, _VP]),
+    "knn_merge": (_I, [_VP, _VP, _I64, _I, _I, _I, _VP, _VP, _VP]),
     "ivfpq_device_check": (_I, [_VP]),
     "ivfpq_selftest_wait_timeout": (_I, [_I, _VP]),
     "ivfpq_last_error": (C.c_char_p, []),
@@ -280,6 +281,24 @@ def flat_knn(db, queries, k, out_dist=None, out_ids=None, stream=None):
         out_ids = torch.empty((nq, k), dtype=torch.int64, device=queries.device)
     _check("flat_knn", lib().flat_knn(_ptr(db), n, d, _ptr(queries), nq, k, _ptr(out_dist),
                                        _ptr(out_ids), _stream(stream)))
+    return out_dist, out_ids
+
+
+def knn_merge(dists, ids, k, out_dist=None, out_ids=None, stream=None):
+    """k smallest of S shards' results per query. dists fp32 and ids int64,
+    both [S, nq, k_in] on the device; returns ([nq, k] fp32, [nq, k] int64)."""
+    torch = _torch()
+    _need(dists, torch.float32, "dists", 3)
+    _need(ids, torch.int64, "ids", 3)
+    if tuple(ids.shape) != tuple(dists.shape):
+        raise ValueError("knn_merge: dists and ids must have the same shape")
+    S, nq, k_in = dists.shape
+    if out_dist is None:
+        out_dist = torch.empty((nq, k), dtype=torch.float32, device=dists.device)
+    if out_ids is None:
+        out_ids = torch.empty((nq, k), dtype=torch.int64, device=dists.device)
+    _check("knn_merge", lib().knn_merge(_ptr(dists), _ptr(ids), nq, S, k_in, k, _ptr(out_dist),
+                                         _ptr(out_ids), _stream(stream)))
     return out_dist, out_ids
 
 

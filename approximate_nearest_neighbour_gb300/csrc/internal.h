@@ -17,7 +17,9 @@ enum class OutKind {
   Float,    // fp32 value (from an order-preserving key) + int64 column index
   Dist,     // fp32 distance (raw non-negative key) + int64 id looked up in id_map
   Probes,   // int32 column index + optional fp32 value
-  Partial   // raw (key, index) pairs, k per (row, chunk)
+  Partial,  // raw (key, index) pairs, k per (row, chunk)
+  Merge     // fp32 value (order-preserving key) + int64 id of candidate c of row r:
+            // id_map[((c / merge_kin) * merge_rows + r) * merge_kin + c % merge_kin]
 };
 
 struct SelectOut {
@@ -29,6 +31,8 @@ struct SelectOut {
   uint32_t* pkeys = nullptr;      // Partial: [rows][chunks][k]
   uint32_t* pidx = nullptr;
   const int* row_mask = nullptr;  // if set, rows with row_mask[row] == 0 are skipped
+  int64_t merge_rows = 0;         // Merge: rows per input set
+  int merge_kin = 0;              // Merge: candidates per row per input set
 };
 
 // Rows of fp32 values: row r holds vals[r*cols .. r*cols+cols). The columns of

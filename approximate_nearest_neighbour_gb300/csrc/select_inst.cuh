@@ -33,6 +33,15 @@ struct OutWriter {
         if (o.vals) o.vals[p] = key_to_float(key);
         break;
       }
+      case OutKind::Merge: {
+        int64_t p = row * k + i;
+        o.vals[p] = key_to_float(key);
+        o.idx64[p] = v == kSentinelIdx
+                         ? int64_t(-1)
+                         : o.id_map[(int64_t(v / o.merge_kin) * o.merge_rows + row) * o.merge_kin +
+                                    v % o.merge_kin];
+        break;
+      }
       case OutKind::Partial: {
         int64_t p = (row * chunks + chunk) * k + i;
         o.pkeys[p] = key;

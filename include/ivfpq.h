@@ -227,6 +227,23 @@ int kselect(const float* vals, int64_t rows, int64_t cols, int k, float* out_val
 int kselect_noalloc(const float* vals, int64_t rows, int64_t cols, int k, float* out_vals,
                     int64_t* out_idx, void* stream);
 
+/*
+ * knn_merge -- final k-selection over the results of S index shards.
+ * Source: sharding ("Billion-scale similarity search with GPUs", section 5,
+ * multi-GPU): every shard holds part of the database and answers all queries;
+ * an additional round of k-selection combines their k results per query.
+ *  dists   device fp32 [nshards, nq, k_in]: shard s's distances of query q,
+ *          ascending or not (order is not required); +inf marks a missing entry
+ *  ids     device int64 [nshards, nq, k_in]: the matching ids (global ids,
+ *          -1 for missing entries)
+ *  k       1 .. IVFPQ_MAX_K; k > nshards * k_in pads with (+inf, -1)
+ *  out_dist device fp32 [nq, k], out_ids device int64 [nq, k]: the k smallest
+ *          distances of each query over all shards, ascending, with their ids
+ * Ties are broken arbitrarily. Errors: INVALID_ARG, OOM, CUDA.
+ */
+int knn_merge(const float* dists, const int64_t* ids, int64_t nq, int nshards, int k_in, int k,
+              float* out_dist, int64_t* out_ids, void* stream);
+
 /* ivfpq_device_check -- synchronises `stream` and reports whether any kernel
  * of this library on the current device gave up a bounded wait since the
  * last check (the tensor-core distance pipeline waits on its own copies and
