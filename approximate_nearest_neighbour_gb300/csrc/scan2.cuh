@@ -120,6 +120,7 @@ ivfpq_scan2_kernel(const ScanParams p) {
   __syncthreads();
 
   if (tid == 0 && n > 0 && s_list[0] >= 0) prefetch_list(p, s_list[0], m);
+  if (tid == 0 && n > 1 && s_list[1] >= 0) prefetch_list(p, s_list[1], m);
   if (n > 0 && s_list[0] >= 0) build(s_list[0], buf0);
   uint32_t c0[MW], c1[MW];
   if (n > 0 && warp < (s_len[0] + 31) >> 5)
@@ -130,9 +131,10 @@ ivfpq_scan2_kernel(const ScanParams p) {
     float* cur = (i & 1) ? buf1 : buf0;
     float* nxt = (i & 1) ? buf0 : buf1;
     if (i + 1 < n) {
-      // one list ahead: a measured optimum (none 20.0 ms, one 15.8 ms, two 16.0 ms,
-      // four 16.5 ms on 2e8 vectors x 10,000 queries x 64 probes)
-      if (tid == 0 && s_list[i + 1] >= 0) prefetch_list(p, s_list[i + 1], m);
+      // two lists ahead (2e8 vectors x 10,000 queries x 64 probes, scan ms: none
+      // 20.0, one 15.8-16.8 depending on the GPU, two 16.0-16.05 on every GPU
+      // measured, four 16.5)
+      if (tid == 0 && i + 2 < n && s_list[i + 2] >= 0) prefetch_list(p, s_list[i + 2], m);
       if (s_list[i + 1] >= 0) build(s_list[i + 1], nxt);
     }
     const int len = s_len[i];
