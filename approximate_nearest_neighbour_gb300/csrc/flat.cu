@@ -63,7 +63,7 @@ int rerank(const float* Q, const float* X, int d, int64_t rows, int k, const Sel
   return select_pairs(rk, rc, rows, k, k, 1, k, o, s);
 }
 
-// Filtered plan (k <= 256, large n). A first tensor-core pass over the
+// Filtered plan (any k <= IVFPQ_MAX_K, large n). A first tensor-core pass over the
 // first ns columns takes, per row, the minimum of u = D - ||q||^2 over each of
 // G >= 4k column groups; the k-th smallest of those G minima is an upper
 // bound on the row's k-th smallest u over all n columns (it is attained by k
@@ -76,7 +76,7 @@ struct FilterPlan {
 };
 
 bool filter_plan(int64_t n, int k, FilterPlan* fp) {
-  if (k > 256 || n < 16384) return false;
+  if (k > IVFPQ_MAX_K || n < 2048) return false;
   const int64_t ns = ceil_div(ceil_div(n, 8), 128) * 128;
   const int split_a = int(ceil_div(4 * int64_t(k), 128));
   if (ns / 128 < split_a || 2 * ns > n) return false;

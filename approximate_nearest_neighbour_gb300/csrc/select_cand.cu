@@ -1,86 +1,17 @@
-// k-selection over the per-row candidate segments of the filtered tensor-core
-// distance pass (gemm_tc.cu, l2_tc_filter): BlockSelect over the valid
-// entries of each row's segments. A row with an overflowed segment (more
-// entries found than it holds) is selected instead over exact distances
-// sum_t (q_t - x_t)^2 to every column, computed here; the caller re-ranks the
-// winners in that exact form anyway.
-//
-// Source: BlockSelect / WarpSelect ("Billion-scale similarity search with
-// GPUs", section 4); exact search by distance tiles (same paper, section 5).
-#include "select_inst.cuh"
+// Candidate selection entry (see select_cand.cuh); queue lengths above 256
+// are instantiated in select_cand_large.cu.
+#include "select_cand.cuh"
 
 namespace ivfpq {
-namespace {
-
-constexpr int kCandWarps = 4;
-
-template <int K, int NW>
-__global__ void __launch_bounds__(NW * 32)
-cand_select_kernel(const uint64_t* __restrict__ cand, const int* __restrict__ scnt, int nseg,
-                   int cap_s, const float* __restrict__ Q, const float* __restrict__ X, int64_t n,
-                   int d, OutWriter out) {
-  constexpr int T = ThreadQ<K>::value;
-  extern __shared__ uint32_t sm_cand[];
-  const int64_t row = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int* cnt = scnt + row * nseg;
-  int over = 0;
-  for (int g = threadIdx.x; g < nseg; g += NW * 32) over |= cnt[g] > cap_s;
-  over = __syncthreads_or(over);
-  WarpSelect<K, T> ws;
-  ws.init(lane);
-  if (!over) {
-    for (int g = warp; g < nseg; g += NW) {
-      const int ns = max(cnt[g], 0);
-      const uint64_t* e = cand + (row * nseg + g) * cap_s;
-      for (int base = 0; base < ns; base += 32) {
-        const int i = base + lane;
-        const bool ok = i < ns;
-        const uint64_t v = ok ? __ldcs(e + i) : ~uint64_t(0);
-        ws.add(uint32_t(v >> 32), uint32_t(v));
-      }
-    }
-  } else {
-    const float* qr = Q + row * d;
-    const int64_t step = int64_t(NW) * 32;
-    for (int64_t base = 0; base < n; base += step) {
-      const int64_t c = base + warp * 32 + lane;
-      const bool ok = c < n;
-      float s = 0.f;
-      if (ok) {
-        const float* xr = X + c * d;
-        for (int t = 0; t < d; ++t) {
-          const float df = __ldg(qr + t) - __ldg(xr + t);
-          s = fmaf(df, df, s);
-        }
-      }
-      ws.add(ok ? float_to_key(s) : kSentinelKey, ok ? uint32_t(c) : kSentinelIdx);
-    }
-  }
-  ws.finalize();
-  block_merge<K, T, NW>(ws, sm_cand, sm_cand + NW * K, warp);
-  if (warp == 0) {
-#pragma unroll
-    for (int r = 0; r < K / 32; ++r) {
-      const int i = 32 * r + lane;
-      if (i < out.k) out.write(row, 0, i, ws.wk[r], ws.wv[r]);
-    }
-  }
-}
-
-template <int K>
-int launch_cand(const uint64_t* cand, const int* scnt, int nseg, int cap_s, int64_t rows,
-                const float* Q, const float* X, int64_t n, int d, const OutWriter& w,
-                cudaStream_t s) {
-  constexpr int NW = kCandWarps;
-  const size_t smem = size_t(NW) * K * 2 * sizeof(uint32_t);
-  auto kern = cand_select_kernel<K, NW>;
-  kern<<<unsigned(rows), NW * 32, smem, s>>>(cand, scnt, nseg, cap_s, Q, X, n, d, w);
-  IVFPQ_LAUNCHED_K(kern, smem, NW * 32);
-  return IVFPQ_OK;
-}
-
-}  // namespace
+extern template int launch_cand<512>(const uint64_t*, const int*, int, int, int64_t,
+                                     const float*, const float*, int64_t, int,
+                                     const OutWriter&, cudaStream_t);
+extern template int launch_cand<1024>(const uint64_t*, const int*, int, int, int64_t,
+                                      const float*, const float*, int64_t, int,
+                                      const OutWriter&, cudaStream_t);
+extern template int launch_cand<2048>(const uint64_t*, const int*, int, int, int64_t,
+                                      const float*, const float*, int64_t, int,
+                                      const OutWriter&, cudaStream_t);
 
 int select_candidates(const uint64_t* cand, const int* scnt, int nseg, int cap_s, int64_t rows,
                       const float* Q, const float* X, int64_t n, int d, int k,
@@ -94,8 +25,11 @@ int select_candidates(const uint64_t* cand, const int* scnt, int nseg, int cap_s
     case 64: return launch_cand<64>(cand, scnt, nseg, cap_s, rows, Q, X, n, d, w, s);
     case 128: return launch_cand<128>(cand, scnt, nseg, cap_s, rows, Q, X, n, d, w, s);
     case 256: return launch_cand<256>(cand, scnt, nseg, cap_s, rows, Q, X, n, d, w, s);
+    case 512: return launch_cand<512>(cand, scnt, nseg, cap_s, rows, Q, X, n, d, w, s);
+    case 1024: return launch_cand<1024>(cand, scnt, nseg, cap_s, rows, Q, X, n, d, w, s);
+    case 2048: return launch_cand<2048>(cand, scnt, nseg, cap_s, rows, Q, X, n, d, w, s);
   }
-  set_error("candidate selection supports k <= 256 (k = %d)", k);
+  set_error("candidate selection supports k <= %d (k = %d)", IVFPQ_MAX_K, k);
   return IVFPQ_ERR_UNSUPPORTED;
 }
 

@@ -52,9 +52,15 @@ def parse():
     p.add_argument("--nq", type=int, default=None)
     p.add_argument("--nlist", type=int, default=None, help="list count override (development)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--workload", default="large", choices=sorted(WORKLOADS),
+                   help="large (default, the headline), mid, billion, or flat (exact k-NN)")
+    p.add_argument("--k", type=int, default=None, help="k override")
     return p.parse_args()
 
 
+# workload -> (shape, nprobe, k); "large" is the configuration the scan target is quoted on
+WORKLOADS = {"large": (S.IVFPQ_LARGE, 64, 100), "mid": (S.IVFPQ_MID, 64, 100),
+             "billion": (S.IVFPQ_BILLION, 128, 100), "flat": (S.FLAT_1M, 0, 100)}
 WORKLOAD = S.IVFPQ_LARGE
 NPROBE, K = 64, 100
 
@@ -315,7 +321,8 @@ def run_ours(args):
         scan_ms = sums[2] / max(count, 1)
         achieved = scan_bytes / (scan_ms / 1e3) / 1e9
         traffic = profiled_traffic(scan_kernel)
-        if traffic is not None and (args.n is not None or args.nlist is not None):
+        if traffic is not None and (args.n is not None or args.nlist is not None
+                                    or args.workload != "large"):
             traffic = None
         total_q = nq * world * args.steps
         line = {
@@ -347,9 +354,157 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ---------------------------------------------------------------------------
+# exact k-NN (flat) workload: 1e6 x 128 database, 10,000 queries
+FALLBACK_BF16_TFLOPS = 1900.0
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense TF32 / bf16 ratio
+
+
+def tf32_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]) * TF32_PER_BF16, "measured bf16_tflops x 1.1/2.25"
+    return FALLBACK_BF16_TFLOPS * TF32_PER_BF16, "fallback bf16 x 1.1/2.25"
+
+
+def flat_config(args, n, nq, d):
+    return {"workload": WORKLOAD.name if args.n is None else f"{WORKLOAD.name}(N={n})", "n": n,
+            "d": d, "nq_per_gpu": nq, "k": K, "parallelism": f"replicas x{args.gpus}",
+            "l2": f"database {n * d * 4 / 1e9:.2f} GB fp32 + {2 * n * 128 * 4 / 1e9:.2f} GB "
+                  f"tensor-core operands, above L2"}
+
+
+def run_flat(args):
+    import torch
+    import torch.distributed as dist
+    from approximate_nearest_neighbour_gb300 import binding as B
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    db, q = S.flat_database(WORKLOAD, n=args.n, nq=args.nq)
+    n, d = db.shape
+    nq = q.shape[0]
+    dbd = torch.from_numpy(db).to(dev)
+    qd = torch.from_numpy(q).to(dev)
+    out_d = torch.empty((nq, K), dtype=torch.float32, device=dev)
+    out_i = torch.empty((nq, K), dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        B.flat_knn(dbd, qd, K, out_d, out_i)
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    launches0 = B.kernel_launches()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        B.flat_knn(dbd, qd, K, out_d, out_i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    launches = B.kernel_launches() - launches0
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    # end to end: pinned host queries in, host results out (database resident)
+    qh = torch.from_numpy(q).pin_memory()
+    hd = torch.empty((nq, K), dtype=torch.float32).pin_memory()
+    hi = torch.empty((nq, K), dtype=torch.int64).pin_memory()
+    qbuf = torch.empty_like(qd)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        qbuf.copy_(qh, non_blocking=True)
+        B.flat_knn(dbd, qbuf, K, out_d, out_i)
+        hd.copy_(out_d, non_blocking=True)
+        hi.copy_(out_i, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e = e0.elapsed_time(e1) / 1e3
+    if rank == 0:
+        peak, src = tf32_peak()
+        call_s = elapsed / args.steps
+        # 3xTF32: three TF32 products of 2 * d flops per (query, database row)
+        flops = 3.0 * 2.0 * d * n * nq
+        achieved = flops / call_s / 1e12
+        line = {
+            "metric": f"flat k-NN queries/s (k={K})", "value": nq * world * args.steps / elapsed,
+            "unit": "queries/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * call_s, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32 (3xTF32 products)", "data": "synthetic",
+            "config": flat_config(args, n, nq, d),
+            "roofline": {"bound": "tensor", "kernel": "flat_knn (all kernels of one call)",
+                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "peak_source": src, "traffic": None,
+                         "algorithmic_flops_per_call": flops},
+            "e2e": {"value": nq * world * args.steps / e2e, "unit": "queries/s",
+                    "h2d_bytes_per_step": int(q.nbytes),
+                    "d2h_bytes_per_step": int(hd.numel() * 4 + hi.numel() * 8)},
+            "gpu_launches": launches, "clocks": clk,
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = flat_cpu_baseline(db, q)
+        emit(line)
+
+
+def flat_cpu_baseline(db, q, target_s=10.0):
+    import oracle
+    threads = oracle.NTHREADS
+    m = min(2 * threads, q.shape[0])
+    t0 = time.perf_counter()
+    oracle.flat_knn(db, q[:m], K)
+    dt = time.perf_counter() - t0
+    nsel = int(min(q.shape[0], max(m, target_s / max(dt, 1e-6) * m)))
+    t0 = time.perf_counter()
+    oracle.flat_knn(db, q[:nsel], K)
+    dt = time.perf_counter() - t0
+    return {"value": nsel / dt, "unit": "queries/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {nsel} of the {q.shape[0]} queries, full database, "
+                      f"{threads} threads, {dt:.1f} s"}
+
+
+def run_flat_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    db, q = S.flat_database(WORKLOAD, n=args.n, nq=args.nq)
+    b = flat_cpu_baseline(db, q, target_s=max(1.0, 10.0 / max(args.steps, 1)))
+    emit({"impl": "reference", "metric": f"flat k-NN queries/s (k={K})", "value": b["value"],
+          "unit": "queries/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+          "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+          "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+          "config": flat_config(args, db.shape[0], q.shape[0], db.shape[1]), "cpu_baseline": b,
+          "e2e": {"value": b["value"], "unit": "queries/s", "h2d_bytes_per_step": 0,
+                  "d2h_bytes_per_step": 0}})
+
+
 def main():
+    global WORKLOAD, NPROBE, K
     args = parse()
-    if args.impl == "reference":
+    WORKLOAD, NPROBE, K = WORKLOADS[args.workload]
+    if args.k is not None:
+        K = args.k
+    if args.workload == "flat":
+        if args.impl == "reference":
+            run_flat_reference(args)
+        else:
+            run_flat(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -24,7 +24,9 @@ def _flat(B, db, q, k):
 
 
 @pytest.mark.parametrize("n,d,nq,k", [(1000, 128, 37, 1), (5000, 128, 64, 100), (3001, 96, 5, 1024),
-                                      (257, 64, 130, 300), (100, 16, 3, 2048), (20_000, 128, 300, 10)])
+                                      (257, 64, 130, 300), (100, 16, 3, 2048), (20_000, 128, 300, 10),
+                                      (40_000, 64, 200, 700), (70_000, 32, 20, 2048),
+                                      (2_500, 96, 150, 20)])
 def test_flat_small(B, n, d, nq, k):
     db, q = S.flat_database(S.FLAT_1M, n=n, nq=nq)
     db = db[:, :d].copy()
@@ -46,7 +48,7 @@ def test_flat_full_size_sampled(B, k):
     compare_knn(gd[rows], gi[rows], od, oi, context=f"flat full k={k}")
 
 
-@pytest.mark.parametrize("k", [10, 64])
+@pytest.mark.parametrize("k", [10, 64, 300])
 def test_flat_filtered_plan_overflow_rows(B, k):
     """The first 4,096 database rows (more than the first pass of the
     filtered plan looks at) lie far from every query, so the bound it takes
