@@ -122,9 +122,17 @@ ivfpq_scan2_kernel(const ScanParams p) {
   if (tid == 0 && n > 0 && s_list[0] >= 0) prefetch_list(p, s_list[0], m);
   if (tid == 0 && n > 1 && s_list[1] >= 0) prefetch_list(p, s_list[1], m);
   if (n > 0 && s_list[0] >= 0) build(s_list[0], buf0);
-  uint32_t c0[MW], c1[MW];
-  if (n > 0 && warp < (s_len[0] + 31) >> 5)
-    load_codes<MW>(p.codes + (s_boff[0] + warp) * 32 * m, lane, c0);
+  // R = 8 / MW blocks per warp and iteration (blocks b, b + 16, ..., all
+  // congruent to the warp mod 16): the same code registers for every m, R
+  // independent sums, the loop overhead shared by R blocks
+  constexpr int R = MW >= 8 ? 1 : 8 / MW;
+  uint32_t c0[R][MW], c1[R][MW];
+  auto load_group = [&](const uint8_t* lc, int b, int nb, uint32_t (&c)[R][MW]) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      if (b + r * NW < nb) load_codes<MW>(lc + int64_t(b + r * NW) * 32 * m, lane, c[r]);
+  };
+  if (n > 0) load_group(p.codes + s_boff[0] * 32 * m, warp, (s_len[0] + 31) >> 5, c0);
   __syncthreads();
 
   for (int i = 0; i < n; ++i) {
@@ -142,18 +150,25 @@ ivfpq_scan2_kernel(const ScanParams p) {
     const int nb = (len + 31) >> 5;
     const uint8_t* lcodes = p.codes + boff * 32 * m;
     const char* lut_bytes = reinterpret_cast<const char*>(cur);
-    for (int b = warp; b < nb; b += NW) {
-      const int bn = b + NW;
-      if (bn < nb) load_codes<MW>(lcodes + int64_t(bn) * 32 * m, lane, c1);
-      const float dist = adc_sum<MW, IVFPQ_LUT_FP32>(c0, lut_bytes, lane4);
-      const bool valid = b * 32 + lane < len;
-      ws.add(valid ? __float_as_uint(dist) : kSentinelKey, uint32_t((boff + b) * 32 + lane));
+    for (int b = warp; b < nb; b += R * NW) {
+      load_group(lcodes, b + R * NW, nb, c1);
 #pragma unroll
-      for (int w = 0; w < MW; ++w) c0[w] = c1[w];
+      for (int r = 0; r < R; ++r) {
+        const int br = b + r * NW;  // the same in every lane
+        if (br < nb) {
+          const float dist = adc_sum<MW, IVFPQ_LUT_FP32>(c0[r], lut_bytes, lane4);
+          const bool valid = br * 32 + lane < len;
+          ws.add(valid ? __float_as_uint(dist) : kSentinelKey,
+                 uint32_t((boff + br) * 32 + lane));
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int w = 0; w < MW; ++w) c0[r][w] = c1[r][w];
     }
-    // this warp's first block of the next list, before the barrier
-    if (i + 1 < n && warp < (s_len[i + 1] + 31) >> 5)
-      load_codes<MW>(p.codes + (s_boff[i + 1] + warp) * 32 * m, lane, c0);
+    // this warp's first blocks of the next list, before the barrier
+    if (i + 1 < n) load_group(p.codes + s_boff[i + 1] * 32 * m, warp, (s_len[i + 1] + 31) >> 5, c0);
     __syncthreads();  // cur may be overwritten next; nxt is complete
   }
   ws.finalize();
