@@ -99,7 +99,8 @@ def test_tiny_workload_trained_codebooks(B):
     assert r > 0.3
 
 
-@pytest.mark.parametrize("m,dsub", [(8, 12), (12, 4), (16, 8), (32, 3), (64, 2), (20, 3), (4, 5)])
+@pytest.mark.parametrize("m,dsub", [(8, 12), (12, 4), (16, 8), (32, 3), (64, 2), (20, 3), (4, 5),
+                                    (8, 8), (16, 4), (32, 4)])
 def test_code_widths_and_ragged_lists(B, m, dsub):
     d = m * dsub
     w = S.IVFPQWorkload("t", 90 + m, 30_000, d, 97, m, 0.15, True, 40, (7,), (33,), ("fp32",))
