@@ -43,6 +43,8 @@ SIGNATURES = {
     "ivfpq_set_profiling": (_I, [_VP, _I]),
     "ivfpq_stage_times": (_I, [_VP, C.POINTER(C.c_float), C.POINTER(C.c_int)]),
     "ivfpq_last_scan_kernel": (C.c_char_p, [_VP]),
+    "ivfpq_set_precomputed": (_I, [_VP, _I]),
+    "ivfpq_uses_precomputed": (_I, [_VP]),
     "ivfpq_kernel_launches": (C.c_uint64, []),
     "flat_knn": (_I, [_VP, _I64, _I, _VP, _I64, _I, _VP, _VP, _VP]),
     "kselect": (_I, [_VP, _I64, _I64, _I, _VP, _VP, _VP]),
@@ -240,6 +242,17 @@ def ivfpq_stage_times(index):
     n = C.c_int(0)
     _check("ivfpq_stage_times", lib().ivfpq_stage_times(index.handle, buf, C.byref(n)))
     return list(buf), n.value
+
+
+def ivfpq_set_precomputed(index, mode):
+    """-1 automatic, 0 off, 1 on (where supported) for the precomputed-term
+    lookup tables; returns whether searches now use them."""
+    _check("ivfpq_set_precomputed", lib().ivfpq_set_precomputed(index.handle, int(mode)))
+    return bool(lib().ivfpq_uses_precomputed(index.handle))
+
+
+def ivfpq_uses_precomputed(index):
+    return bool(lib().ivfpq_uses_precomputed(index.handle))
 
 
 def last_scan_kernel(index):

@@ -101,6 +101,12 @@ int tc_filter_split(int64_t nq, int64_t n);
 int select_candidates(const uint64_t* cand, const int* scnt, int nseg, int cap_s, int64_t rows,
                       const float* Q, const float* X, int64_t n, int d, int k,
                       const SelectOut& out, cudaStream_t s);
+// Whether searches of this index use the precomputed-term tables (the
+// register-codebook scan, fp32 tables, m <= 16 when automatic), and their
+// construction (ivfpq_index.cu).
+bool use_precomputed(const ivfpq_index* ix);
+int build_term1(ivfpq_index* ix);
+
 // ---- flat / coarse search on distance tiles (flat.cu) ----------------------------
 // k nearest rows of X for each row of Q under squared L2; output as SelectOut
 // (Float with column ids, or Probes).
@@ -119,6 +125,11 @@ struct ivfpq_index {
   float* centroids = nullptr;   // [nlist, d]
   float* cent_norms = nullptr;  // [nlist]
   float* codebooks = nullptr;   // [256, m, dsub4], zero-padded to dsub4 = roundup(dsub, 4)
+  // precomputed list terms ||y_R||^2 + 2 <y_C, y_R> per (list, reproduction
+  // value, sub-quantizer), [nlist, 256, m]; null unless the precomputed-term
+  // tables are in use (precomputed: -1 automatic, 0 off, 1 on)
+  float* term1 = nullptr;
+  int precomputed = -1;
   // tensor-core operands of the centroids (null when that path is unavailable)
   float* cent_hi = nullptr;     // [nlist, tc_dpad(d)]
   float* cent_lo = nullptr;

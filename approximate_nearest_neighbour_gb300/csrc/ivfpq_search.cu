@@ -30,29 +30,40 @@ IVFPQ_EXTERN_SCAN(16, 64)
 IVFPQ_EXTERN_SCAN(16, 128)
 IVFPQ_EXTERN_SCAN(16, 256)
 
-#define IVFPQ_EXTERN_SCAN2(MW, DS)                                                         \
-  extern template int launch_scan2<MW, DS, 32>(const ScanParams&, int64_t, cudaStream_t); \
-  extern template int launch_scan2<MW, DS, 64>(const ScanParams&, int64_t, cudaStream_t);
-IVFPQ_EXTERN_SCAN2(8, 3)
-IVFPQ_EXTERN_SCAN2(8, 4)
+#define IVFPQ_EXTERN_SCAN2_1(MW, DS, KW, PRE) \
+  extern template int launch_scan2<MW, DS, KW, PRE>(const ScanParams&, int64_t, cudaStream_t);
+#define IVFPQ_EXTERN_SCAN2(MW, DS)                                                        \
+  IVFPQ_EXTERN_SCAN2_1(MW, DS, 32, false) IVFPQ_EXTERN_SCAN2_1(MW, DS, 64, false)         \
+  IVFPQ_EXTERN_SCAN2_1(MW, DS, 32, true) IVFPQ_EXTERN_SCAN2_1(MW, DS, 64, true)
+IVFPQ_EXTERN_SCAN2_1(8, 3, 32, false)
+IVFPQ_EXTERN_SCAN2_1(8, 3, 64, false)
+IVFPQ_EXTERN_SCAN2_1(8, 4, 32, false)
+IVFPQ_EXTERN_SCAN2_1(8, 4, 64, false)
 IVFPQ_EXTERN_SCAN2(4, 8)
 IVFPQ_EXTERN_SCAN2(4, 4)
 IVFPQ_EXTERN_SCAN2(2, 12)
 IVFPQ_EXTERN_SCAN2(2, 8)
 
 // The register-codebook kernel (scan2.cuh) with KW-entry warp queues, for
-// the (m, d/m) shapes it is built for; 1 = launched, 0 = not applicable.
+// the (m, d/m) shapes it is built for, with precomputed-term tables when
+// p.term1 is set (m <= 16 shapes); 1 = launched, 0 = not applicable.
 template <int KW>
 int try_scan2_kw(const ScanParams& p, int64_t nq, cudaStream_t s, int* launched) {
   *launched = 1;
   const int key = p.m * 100 + p.dsub;
+  const bool pre = p.term1 != nullptr;
   switch (key) {
-    case 3203: return launch_scan2<8, 3, KW>(p, nq, s);
-    case 3204: return launch_scan2<8, 4, KW>(p, nq, s);
-    case 1608: return launch_scan2<4, 8, KW>(p, nq, s);
-    case 1604: return launch_scan2<4, 4, KW>(p, nq, s);
-    case 812: return launch_scan2<2, 12, KW>(p, nq, s);
-    case 808: return launch_scan2<2, 8, KW>(p, nq, s);
+    case 3203: return launch_scan2<8, 3, KW, false>(p, nq, s);
+    case 3204: return launch_scan2<8, 4, KW, false>(p, nq, s);
+    case 1608:
+      return pre ? launch_scan2<4, 8, KW, true>(p, nq, s) : launch_scan2<4, 8, KW, false>(p, nq, s);
+    case 1604:
+      return pre ? launch_scan2<4, 4, KW, true>(p, nq, s) : launch_scan2<4, 4, KW, false>(p, nq, s);
+    case 812:
+      return pre ? launch_scan2<2, 12, KW, true>(p, nq, s)
+                 : launch_scan2<2, 12, KW, false>(p, nq, s);
+    case 808:
+      return pre ? launch_scan2<2, 8, KW, true>(p, nq, s) : launch_scan2<2, 8, KW, false>(p, nq, s);
   }
   *launched = 0;
   return IVFPQ_OK;
@@ -181,6 +192,7 @@ int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int npro
   p.nprobe = nprobe;
   p.k = k;
   p.lut_type = ix->lut_type;
+  if (use_precomputed(ix)) p.term1 = ix->term1;
   plan_chunks(nq, nprobe, &p.per_chunk, &p.nchunks);
   Workspace ws(s);
   SelectOut o;

@@ -50,6 +50,7 @@ struct ScanParams {
   int d, m, dsub, dsub4, nlist, nprobe, per_chunk, nchunks, k;
   int lut_type;              // IVFPQ_LUT_FP32 / FP16 / FP8
   const int* qmask = nullptr;  // if set, only queries q with qmask[q] != 0 are scanned
+  const float* term1 = nullptr;  // precomputed list terms [nlist, 256, m] (register-codebook scan)
 };
 
 constexpr int kScanWarps = 8;

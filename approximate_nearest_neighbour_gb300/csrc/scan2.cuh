@@ -47,7 +47,7 @@ struct Scan2Shape {
   static constexpr int DS4 = (DS + 3) & ~3;
 };
 
-template <int MW, int DS, int KW>
+template <int MW, int DS, int KW, bool PRE>
 __global__ void __launch_bounds__(kScan2Warps * 32, 1)
 ivfpq_scan2_kernel(const ScanParams p) {
   using Sh = Scan2Shape<MW, DS>;
@@ -78,20 +78,42 @@ ivfpq_scan2_kernel(const ScanParams p) {
 #pragma unroll
   for (int t = 0; t < DS; ++t) xs[t] = __ldg(x + t);
 
-  // table of list l into buf (fp32 entries, one per 4-byte slot)
+  // precomputed terms: this thread's entries of the query's table
+  // -2 <x^(jj), y_R(e)> (the codewords are not needed after this)
+  float t3[PRE ? Sh::STEPS : 1];
+  if constexpr (PRE) {
+#pragma unroll
+    for (int s = 0; s < Sh::STEPS; ++s) {
+      float a = 0.f;
+#pragma unroll
+      for (int t = 0; t < DS; ++t) a = fmaf(xs[t], cw[s][t], a);
+      t3[s] = -2.f * a;
+    }
+  }
+
+  // table of list l into buf (fp32 entries, one per 4-byte slot): the direct
+  // ||r^(jj) - y_R(e)||^2, or with precomputed terms T1[l][e][jj] + t3 (the
+  // list's ||x - y_C||^2 is added to every distance of the list instead)
   auto build = [&](int l, float* buf) {
     const float* cl = p.centroids + int64_t(l) * p.d + jj * DS;
     float r[DS];
+    if constexpr (!PRE) {
 #pragma unroll
-    for (int t = 0; t < DS; ++t) r[t] = xs[t] - __ldg(cl + t);
+      for (int t = 0; t < DS; ++t) r[t] = xs[t] - __ldg(cl + t);
+    }
+    const float* t1 = p.term1 + int64_t(l) * 256 * m + jj;
 #pragma unroll
     for (int s = 0; s < Sh::STEPS; ++s) {
       const int e = (s * NW + warp) * Sh::QQ + qq;
       float Tv = 0.f;
+      if constexpr (PRE) {
+        Tv = __ldg(t1 + e * m) + t3[s];
+      } else {
 #pragma unroll
-      for (int t = 0; t < DS; ++t) {
-        const float df = r[t] - cw[s][t];
-        Tv = fmaf(df, df, Tv);
+        for (int t = 0; t < DS; ++t) {
+          const float df = r[t] - cw[s][t];
+          Tv = fmaf(df, df, Tv);
+        }
       }
       float* row = buf + e * 64 + jj;
 #pragma unroll
@@ -110,12 +132,31 @@ ivfpq_scan2_kernel(const ScanParams p) {
   int* s_list = reinterpret_cast<int*>(scan2_smem + 2 * kGroupWords);
   int* s_len = s_list + kScan2MaxLists;
   int64_t* s_boff = reinterpret_cast<int64_t*>(s_len + kScan2MaxLists);
+  float* s_c2 = reinterpret_cast<float*>(s_boff + kScan2MaxLists);
   for (int i = tid; i < n; i += NW * 32) {
     const int l = p.probes[q * p.nprobe + p0 + i];
     const bool v = l >= 0 && l < p.nlist;
     s_list[i] = v ? l : -1;
     s_len[i] = v ? p.list_len[l] : 0;
     s_boff[i] = v ? p.list_block_off[l] : 0;
+  }
+  if constexpr (PRE) {
+    // ||x - y_C||^2 of each list, one warp per list (exact form, fp32)
+    const float* xq = p.queries + q * p.d;
+    for (int i = warp; i < n; i += NW) {
+      const int l = p.probes[q * p.nprobe + p0 + i];
+      float a = 0.f;
+      if (l >= 0 && l < p.nlist) {
+        const float* c = p.centroids + int64_t(l) * p.d;
+        for (int t = lane; t < p.d; t += 32) {
+          const float df = __ldg(xq + t) - __ldg(c + t);
+          a = fmaf(df, df, a);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o /= 2) a += __shfl_xor_sync(kFullMask, a, o);
+      if (lane == 0) s_c2[i] = a;
+    }
   }
   __syncthreads();
 
@@ -153,13 +194,15 @@ ivfpq_scan2_kernel(const ScanParams p) {
     const int nb = (len + 31) >> 5;
     const uint8_t* lcodes = p.codes + boff * 32 * m;
     const char* lut_bytes = reinterpret_cast<const char*>(cur);
+    const float c2 = PRE ? s_c2[i] : 0.f;
     for (int b = warp; b < nb; b += R * NW) {
       load_group(lcodes, b + R * NW, nb, c1);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const int br = b + r * NW;  // the same in every lane
         if (br < nb) {
-          const float dist = adc_sum<MW, IVFPQ_LUT_FP32>(c0[r], lut_bytes, lane4);
+          float dist = adc_sum<MW, IVFPQ_LUT_FP32>(c0[r], lut_bytes, lane4);
+          if constexpr (PRE) dist = fmaxf(dist + c2, 0.f);  // keys are raw bits of d >= 0
           const bool valid = br * 32 + lane < len;
           ws.add(valid ? __float_as_uint(dist) : kSentinelKey,
                  uint32_t((boff + br) * 32 + lane));
@@ -185,15 +228,15 @@ ivfpq_scan2_kernel(const ScanParams p) {
 }
 
 // two table buffers and the staged probe list
-inline size_t scan2_smem_bytes() { return size_t(2) * kGroupWords * 4 + kScan2MaxLists * 16; }
+inline size_t scan2_smem_bytes() { return size_t(2) * kGroupWords * 4 + kScan2MaxLists * 20; }
 
 // Warp-queue length for a result of k <= 256: each warp's share of the k
 // best is about k / 16, so 32 entries (64 for k > 128) leave a wide margin.
 inline int scan2_kw(int k) { return k <= 128 ? 32 : 64; }
 
-template <int MW, int DS, int KW>
+template <int MW, int DS, int KW, bool PRE>
 int launch_scan2(const ScanParams& p, int64_t nq, cudaStream_t s) {
-  auto kern = ivfpq_scan2_kernel<MW, DS, KW>;
+  auto kern = ivfpq_scan2_kernel<MW, DS, KW, PRE>;
   const size_t smem = scan2_smem_bytes();
   IVFPQ_TRY(set_dynamic_smem(kern, smem));
   const int64_t blocks = nq * p.nchunks;
@@ -204,5 +247,6 @@ int launch_scan2(const ScanParams& p, int64_t nq, cudaStream_t s) {
 
 }  // namespace ivfpq
 
-#define IVFPQ_INST_SCAN2(MW, DS, KW) \
-  template int ivfpq::launch_scan2<MW, DS, KW>(const ivfpq::ScanParams&, int64_t, cudaStream_t);
+#define IVFPQ_INST_SCAN2(MW, DS, KW, PRE)                                                  \
+  template int ivfpq::launch_scan2<MW, DS, KW, PRE>(const ivfpq::ScanParams&, int64_t,      \
+                                                    cudaStream_t);

@@ -1,0 +1,7 @@
+// Register-codebook list-scan kernels for m = 16 with precomputed-term tables (see scan2.cuh).
+#include "scan2.cuh"
+
+IVFPQ_INST_SCAN2(4, 8, 32, true)
+IVFPQ_INST_SCAN2(4, 8, 64, true)
+IVFPQ_INST_SCAN2(4, 4, 32, true)
+IVFPQ_INST_SCAN2(4, 4, 64, true)

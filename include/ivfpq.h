@@ -170,6 +170,29 @@ int ivfpq_search_preassigned(const ivfpq_index* index, const float* queries, int
 int ivfpq_set_profiling(ivfpq_index* index, int enable);
 int ivfpq_stage_times(const ivfpq_index* index, float* ms, int* nsearches);
 
+/*
+ * ivfpq_set_precomputed -- lookup tables from precomputed terms.
+ * Source: "Billion-scale similarity search with GPUs", section 5: the
+ * residual distance ||x - y_C - y_R||^2 expands into ||x - y_C||^2 (the
+ * coarse distance, per query and list), ||y_R||^2 + 2 <y_C, y_R> (per list and
+ * code: a table of 256 x m entries per list, computed once) and
+ * -2 <x, y_R> (per query: one table of 256 x m entries for all its lists), so
+ * a list's table is the sum of a stored table and the query's table instead
+ * of 256 x d multiply-adds. The stored tables take nlist x 256 x m x 4 bytes
+ * of device memory.
+ *  mode  -1 automatic (default: on for fp32 tables with m = 16, d/m = 8,
+ *           where it measured faster), 0 off, 1 on where supported (fp32
+ *           tables, m = 8 with d/m in {12, 8}, m = 16 with d/m in {8, 4})
+ * Synchronizes the device; must not overlap a search of the index. Results
+ * equal those of the direct tables up to fp32 rounding (distances are
+ * clamped at 0). Errors: INVALID_ARG, OOM, CUDA.
+ */
+int ivfpq_set_precomputed(ivfpq_index* index, int mode);
+
+/* ivfpq_uses_precomputed -- 1 if searches of the index currently use the
+ * precomputed-term tables, else 0. */
+int ivfpq_uses_precomputed(const ivfpq_index* index);
+
 /* ivfpq_last_scan_kernel -- name of the list-scan kernel family that the
  * most recent search of this index launched ("ivfpq_scan2_kernel": codebook
  * in registers, double-buffered fp32 tables; "ivfpq_scan_kernel": the general

@@ -127,6 +127,31 @@ def test_empty_lists_large_k_and_padding(B):
         assert np.isinf(gd[:, -1]).all() and (gi[:, -1] == -1).all()
 
 
+@pytest.mark.parametrize("m,dsub", [(8, 12), (8, 8), (16, 8), (16, 4)])
+def test_precomputed_term_tables_follow_the_oracle(B, m, dsub):
+    """Tables from precomputed terms (list table + query table + the coarse
+    distance) and the direct tables both match the oracle's direct ADC
+    within the tolerance, on the same probes; automatic mode selects the
+    precomputed tables where they measured faster (m = 16, d/m = 8)."""
+    import torch
+    w = S.IVFPQWorkload("t", 140 + m + dsub, 30_000, m * dsub, 61, m, 0.15, True, 30, (6,),
+                        (40,), ("fp32",))
+    data = S.compressed_index(w)
+    q = S.queries(w.number, data.cent, data.weights, w.sigma, w.nq)
+    ix = make_index(B, data.cent, data.cb, data.codes, data.list_ids, data.ids)
+    assert B.ivfpq_uses_precomputed(ix) == ((m, dsub) == (16, 8))  # automatic mode
+    assert B.ivfpq_set_precomputed(ix, 1)
+    lists = oracle.to_lists(data.codes, data.list_ids, data.ids, w.nlist)
+    gd1, gi1, _ = search_and_check(B, ix, data.cent, data.cb, lists, q, 6, 40,
+                                   context=f"precomputed m={m}")
+    assert not B.ivfpq_set_precomputed(ix, 0)
+    gd0, gi0, _ = search_and_check(B, ix, data.cent, data.cb, lists, q, 6, 40,
+                                   context=f"direct m={m}")
+    assert np.all(np.abs(gd1 - gd0) <= tol(gd0))
+    assert B.ivfpq_set_precomputed(ix, 1)
+    torch.cuda.synchronize()
+
+
 def test_appending_in_pieces_equals_one_add(B):
     import torch
     w = S.IVFPQWorkload("t", 66, 25_000, 64, 64, 16, 0.15, False, 30, (5,), (20,), ("fp32",))
