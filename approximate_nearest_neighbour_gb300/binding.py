@@ -50,6 +50,9 @@ SIGNATURES = {
     "kselect": (_I, [_VP, _I64, _I64, _I, _VP, _VP, _VP]),
     "kselect_noalloc": (_I, [_VP, _I64, _I64, _I, _VP, _VP, _VP]),
     "knn_merge": (_I, [_VP, _VP, _I64, _I, _I, _I, _VP, _VP, _VP]),
+    "kmeans_lloyd": (_I, [_VP, _I64, _I, _I, _I, _VP, _VP, _VP, _VP, _VP]),
+    "pq_train": (_I, [_VP, _I64, _I, _I, _I, _VP, _VP, _VP, _VP]),
+    "ivfpq_encode": (_I, [_VP, _VP, _I64, _VP, _VP, _VP]),
     "ivfpq_device_check": (_I, [_VP]),
     "ivfpq_selftest_wait_timeout": (_I, [_I, _VP]),
     "ivfpq_last_error": (C.c_char_p, []),
@@ -295,6 +298,53 @@ def flat_knn(db, queries, k, out_dist=None, out_ids=None, stream=None):
     _check("flat_knn", lib().flat_knn(_ptr(db), n, d, _ptr(queries), nq, k, _ptr(out_dist),
                                        _ptr(out_ids), _stream(stream)))
     return out_dist, out_ids
+
+
+def kmeans_lloyd(x, init, niter, stream=None):
+    """Lloyd k-means on device fp32 x [n, d] seeded from rows init (int64
+    [k]): (centroids [k, d], assignment int32 [n], objective per pass as a
+    numpy fp64 array of niter + 1)."""
+    import numpy as np
+    torch = _torch()
+    _need(x, torch.float32, "x", 2)
+    _need(init, torch.int64, "init", 1)
+    n, d = x.shape
+    k = init.shape[0]
+    cent = torch.empty((k, d), dtype=torch.float32, device=x.device)
+    assign = torch.empty((n,), dtype=torch.int32, device=x.device)
+    obj = np.zeros(niter + 1, np.float64)
+    _check("kmeans_lloyd", lib().kmeans_lloyd(
+        _ptr(x), n, d, k, niter, _ptr(init), _ptr(cent), _ptr(assign),
+        obj.ctypes.data_as(C.c_void_p), _stream(stream)))
+    return cent, assign, obj
+
+
+def pq_train(x, m, niter, init, stream=None):
+    """Product quantizer codebooks [m, 256, d/m] trained on device fp32 x
+    [n, d], seeded from rows init (int64 [256]); returns (codebooks,
+    objective per pass, numpy fp64 [niter + 1])."""
+    import numpy as np
+    torch = _torch()
+    _need(x, torch.float32, "x", 2)
+    _need(init, torch.int64, "init", 1)
+    n, d = x.shape
+    cb = torch.empty((m, 256, d // m), dtype=torch.float32, device=x.device)
+    obj = np.zeros(niter + 1, np.float64)
+    _check("pq_train", lib().pq_train(_ptr(x), n, d, m, niter, _ptr(init), _ptr(cb),
+                                       obj.ctypes.data_as(C.c_void_p), _stream(stream)))
+    return cb, obj
+
+
+def ivfpq_encode(index, x, stream=None):
+    """(list ids int32 [n], codes uint8 [n, m]) of device fp32 x [n, d]."""
+    torch = _torch()
+    _need(x, torch.float32, "x", 2)
+    n = x.shape[0]
+    lists = torch.empty((n,), dtype=torch.int32, device=x.device)
+    codes = torch.empty((n, index.m), dtype=torch.uint8, device=x.device)
+    _check("ivfpq_encode", lib().ivfpq_encode(index.handle, _ptr(x), n, _ptr(lists),
+                                               _ptr(codes), _stream(stream)))
+    return lists, codes
 
 
 def knn_merge(dists, ids, k, out_dist=None, out_ids=None, stream=None):

@@ -251,6 +251,56 @@ int kselect_noalloc(const float* vals, int64_t rows, int64_t cols, int k, float*
                     int64_t* out_idx, void* stream);
 
 /*
+ * kmeans_lloyd -- Lloyd k-means (coarse quantizer training).
+ * Source: "Billion-scale similarity search with GPUs", section 6: k-means
+ * alternates a k = 1 nearest-centroid search over all points with a centroid
+ * update.
+ *  x          device fp32 [n, d], k <= n < 2^31, d >= 1
+ *  init       device int64 [k]: row indices of x that seed the centroids
+ *  niter      number of updates (>= 0); niter + 1 assignment passes
+ *  centroids  device fp32 [k, d] (out)
+ *  assign     device int32 [n] (out, may be NULL): the final assignment
+ *  objective  HOST fp64 [niter + 1] (out, may be NULL): sum of squared
+ *             distances to the assigned centroid at each assignment pass
+ * The update is the mean of each cluster's points summed in fp64 in
+ * increasing point order (deterministic); an empty cluster keeps its
+ * centroid. Synchronizes `stream`. Errors: INVALID_ARG (also an init index
+ * outside [0, n)), OOM, CUDA.
+ */
+int kmeans_lloyd(const float* x, int64_t n, int d, int k, int niter, const int64_t* init,
+                 float* centroids, int32_t* assign, double* objective, void* stream);
+
+/*
+ * pq_train -- product quantizer training: for each of the m sub-spaces
+ * (dimensions [j*d/m, (j+1)*d/m)), kmeans_lloyd with 256 centroids on the
+ * points' sub-vectors (train on residuals x - centroid of x's list for IVF-PQ).
+ * Source: "Custom 8-bit floating point value format ...", index construction
+ * step 3 (256 codewords per sub-space); "Billion-scale similarity search with
+ * GPUs", sections 5-6.
+ *  x          device fp32 [n, d], 256 <= n < 2^31, d % m == 0
+ *  init       device int64 [256]: the rows whose sub-vectors seed every
+ *             sub-quantizer's codewords
+ *  codebooks  device fp32 [m, 256, d/m] (out), the layout ivfpq_index_create takes
+ *  objective  HOST fp64 [niter + 1] (may be NULL): summed over sub-quantizers
+ * Synchronizes `stream`. Errors: INVALID_ARG, OOM, CUDA.
+ */
+int pq_train(const float* x, int64_t n, int d, int m, int niter, const int64_t* init,
+             float* codebooks, double* objective, void* stream);
+
+/*
+ * ivfpq_encode -- IVF-PQ codes of a batch of vectors, for ivfpq_add.
+ * Source: "Custom 8-bit floating point value format ...", index construction
+ * steps 1-3 (nearest centroid, residual, nearest codeword per sub-space).
+ *  x         device fp32 [n, index d]
+ *  list_ids  device int32 [n] (out): nearest centroid (exact distances)
+ *  codes     device uint8 [n, m] (out): per sub-space, the codeword nearest
+ *            to the residual's sub-vector (fp32 distances, lowest index on ties)
+ * Asynchronous. Errors: INVALID_ARG (also d/m > 32), OOM, CUDA.
+ */
+int ivfpq_encode(const ivfpq_index* index, const float* x, int64_t n, int32_t* list_ids,
+                 uint8_t* codes, void* stream);
+
+/*
  * knn_merge -- final k-selection over the results of S index shards.
  * Source: sharding ("Billion-scale similarity search with GPUs", section 5,
  * multi-GPU): every shard holds part of the database and answers all queries;
