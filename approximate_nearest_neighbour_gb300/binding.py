@@ -53,6 +53,7 @@ SIGNATURES = {
     "kmeans_lloyd": (_I, [_VP, _I64, _I, _I, _I, _VP, _VP, _VP, _VP, _VP]),
     "pq_train": (_I, [_VP, _I64, _I, _I, _I, _VP, _VP, _VP, _VP]),
     "ivfpq_encode": (_I, [_VP, _VP, _I64, _VP, _VP, _VP]),
+    "ivfpq_knn_graph": (_I, [_VP, _VP, _VP, _I64, _I, _I, _VP, _VP, _VP]),
     "ivfpq_device_check": (_I, [_VP]),
     "ivfpq_selftest_wait_timeout": (_I, [_I, _VP]),
     "ivfpq_last_error": (C.c_char_p, []),
@@ -333,6 +334,21 @@ def pq_train(x, m, niter, init, stream=None):
     _check("pq_train", lib().pq_train(_ptr(x), n, d, m, niter, _ptr(init), _ptr(cb),
                                        obj.ctypes.data_as(C.c_void_p), _stream(stream)))
     return cb, obj
+
+
+def ivfpq_knn_graph(index, x, self_ids, nprobe, k, stream=None):
+    """k approximate neighbours of every row of x among the index's other
+    vectors: ([n, k] fp32 distances, [n, k] int64 ids)."""
+    torch = _torch()
+    _need(x, torch.float32, "x", 2)
+    _need(self_ids, torch.int64, "self_ids", 1)
+    n = x.shape[0]
+    d = torch.empty((n, k), dtype=torch.float32, device=x.device)
+    i = torch.empty((n, k), dtype=torch.int64, device=x.device)
+    _check("ivfpq_knn_graph", lib().ivfpq_knn_graph(index.handle, _ptr(x), _ptr(self_ids), n,
+                                                     nprobe, k, _ptr(d), _ptr(i),
+                                                     _stream(stream)))
+    return d, i
 
 
 def ivfpq_encode(index, x, stream=None):

@@ -270,6 +270,30 @@ int check_common(const ivfpq_index* ix, const float* queries, int64_t nq, int np
 
 void reset_events(const ivfpq_index* ix) { begin_profile(ix); }
 
+// Row r of a [rows, k + 1] result without the entry whose id is self[r] (or
+// without its last entry when self[r] is absent) -> [rows, k]. One thread per
+// row.
+__global__ void drop_self_kernel(const float* __restrict__ d1, const int64_t* __restrict__ i1,
+                                 int64_t rows, int k, const int64_t* __restrict__ self,
+                                 float* __restrict__ d, int64_t* __restrict__ id) {
+  const int64_t r = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (r >= rows) return;
+  const int64_t me = self[r];
+  const float* dr = d1 + r * (k + 1);
+  const int64_t* ir = i1 + r * (k + 1);
+  int o = 0;
+  bool dropped = false;
+  for (int j = 0; j <= k && o < k; ++j) {
+    if (!dropped && ir[j] == me && me >= 0) {
+      dropped = true;
+      continue;
+    }
+    d[r * k + o] = dr[j];
+    id[r * k + o] = ir[j];
+    ++o;
+  }
+}
+
 }  // namespace
 }  // namespace ivfpq
 
@@ -291,6 +315,38 @@ extern "C" int ivfpq_search(const ivfpq_index* ix, const float* queries, int64_t
   IVFPQ_TRY(coarse_stage(ix, queries, nq, nprobe, probes, nullptr, s));
   record(ix, 1, s);
   return scan_stage(ix, queries, nq, nprobe, probes, k, out_dist, out_ids, s);
+}
+
+extern "C" int ivfpq_knn_graph(const ivfpq_index* ix, const float* x, const int64_t* self_ids,
+                               int64_t n, int nprobe, int k, float* out_dist, int64_t* out_ids,
+                               void* stream) {
+  clear_error();
+  IVFPQ_TRY(check_common(ix, x, n, nprobe, "ivfpq_knn_graph"));
+  IVFPQ_REQUIRE(k >= 1 && k < IVFPQ_MAX_K, "ivfpq_knn_graph: k=%d outside [1, %d]", k,
+                IVFPQ_MAX_K - 1);
+  if (n == 0) return IVFPQ_OK;
+  IVFPQ_REQUIRE(self_ids && out_dist && out_ids, "ivfpq_knn_graph: null pointer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  reset_events(ix);
+  // batches of queries bound the temporary memory
+  const int64_t batch = std::min<int64_t>(n, 32768);
+  Workspace ws(s);
+  int32_t* probes = nullptr;
+  float* d1 = nullptr;
+  int64_t* i1 = nullptr;
+  IVFPQ_TRY(ws.alloc(&probes, size_t(batch) * nprobe));
+  IVFPQ_TRY(ws.alloc(&d1, size_t(batch) * (k + 1)));
+  IVFPQ_TRY(ws.alloc(&i1, size_t(batch) * (k + 1)));
+  for (int64_t b0 = 0; b0 < n; b0 += batch) {
+    const int64_t rows = std::min(batch, n - b0);
+    const float* xb = x + b0 * ix->d;
+    IVFPQ_TRY(coarse_stage(ix, xb, rows, nprobe, probes, nullptr, s));
+    IVFPQ_TRY(scan_stage(ix, xb, rows, nprobe, probes, k + 1, d1, i1, s));
+    drop_self_kernel<<<unsigned(ceil_div(rows, 256)), 256, 0, s>>>(
+        d1, i1, rows, k, self_ids + b0, out_dist + b0 * k, out_ids + b0 * k);
+    IVFPQ_LAUNCHED();
+  }
+  return IVFPQ_OK;
 }
 
 extern "C" int ivfpq_search_probes(const ivfpq_index* ix, const float* queries, int64_t nq,

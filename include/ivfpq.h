@@ -251,6 +251,21 @@ int kselect_noalloc(const float* vals, int64_t rows, int64_t cols, int k, float*
                     int64_t* out_idx, void* stream);
 
 /*
+ * ivfpq_knn_graph -- approximate k-nearest-neighbour graph of a vector set:
+ * every vector searched as a query against an index holding the same set
+ * ("Billion-scale similarity search with GPUs", section 6, k-NN graph).
+ *  x         device fp32 [n, d]: the vectors (as added to the index)
+ *  self_ids  device int64 [n]: the id under which x[i] was added; that id is
+ *            removed from row i (if the search did not return it, the row's
+ *            (k+1)-th neighbour is dropped instead)
+ *  nprobe, k as ivfpq_search, 1 <= k < IVFPQ_MAX_K
+ *  out_dist  device fp32 [n, k], out_ids device int64 [n, k]
+ * Queries run in batches of 32,768. Errors: as ivfpq_search.
+ */
+int ivfpq_knn_graph(const ivfpq_index* index, const float* x, const int64_t* self_ids, int64_t n,
+                    int nprobe, int k, float* out_dist, int64_t* out_ids, void* stream);
+
+/*
  * kmeans_lloyd -- Lloyd k-means (coarse quantizer training).
  * Source: "Billion-scale similarity search with GPUs", section 6: k-means
  * alternates a k = 1 nearest-centroid search over all points with a centroid

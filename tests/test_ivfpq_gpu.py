@@ -349,3 +349,29 @@ def test_full_large_reduced_table_recall_gates(B, lut, gate):
     print(f"{lut} recall@100 vs fp32 oracle = {r:.4f}")
     assert r >= gate
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("k", [10, 40])
+def test_knn_graph_of_an_exactly_encoded_set(B, k):
+    """Vectors built as centroid + codewords, all lists probed: the ADC
+    distances are the exact ones, so the k-NN graph (each vector's own id
+    removed) is the exact graph of the set."""
+    import torch
+    rng = np.random.default_rng(60 + k)
+    nlist, d, m, n = 12, 32, 8, 3000
+    cent = rng.standard_normal((nlist, d)).astype(np.float32)
+    cb = (0.5 * rng.standard_normal((m, 256, d // m))).astype(np.float32)
+    list_ids = rng.integers(0, nlist, n).astype(np.int32)
+    codes = rng.integers(0, 256, (n, m)).astype(np.uint8)
+    x = (cent[list_ids] + cb[np.arange(m), codes].reshape(n, d)).astype(np.float32)
+    ids = (np.arange(n, dtype=np.int64) * 3 + 1)
+    ix = make_index(B, cent, cb, codes, list_ids, ids)
+    gd, gi = B.ivfpq_knn_graph(ix, _t(x), _t(ids), nlist, k)
+    torch.cuda.synchronize()
+    gd, gi = gd.cpu().numpy(), gi.cpu().numpy()
+    assert not np.any(gi == ids[:, None]), "a vector is its own neighbour"
+    od, oi = oracle.flat_knn(x, x, k + 1 + 64)
+    keep = oi != np.arange(n)[:, None]
+    od2 = np.stack([od[r][keep[r]][:k + 64] for r in range(n)])
+    oi2 = np.stack([ids[oi[r][keep[r]][:k + 64]] for r in range(n)])
+    compare_knn(gd, gi, od2, oi2, context="knn graph")
