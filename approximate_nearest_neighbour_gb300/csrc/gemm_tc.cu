@@ -334,9 +334,14 @@ l2_tc_kernel(const __grid_constant__ CUtensorMap mq_hi, const __grid_constant__ 
         float v[32];
         tmem_ld32(tmem + (uint32_t(32 * lg) << 16) + uint32_t(ab * TN + c * 32), v);
         const int cb = col0 + c * 32;
+        const bool full = cb + 32 <= a.n;
+        // norms of the chunk's columns (0 past n); the filter's full-chunk
+        // path reads them inline instead
         float xn[32];
+        if (MODE != kModeFilter || !full) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) xn[j] = cb + j < a.n ? __ldg(a.xnorm + cb + j) : 0.f;
+          for (int j = 0; j < 32; ++j) xn[j] = cb + j < a.n ? __ldg(a.xnorm + cb + j) : 0.f;
+        }
         if constexpr (MODE == kModeTile) {
           float* drow = a.D + int64_t(q) * a.ldd;
 #pragma unroll
@@ -359,6 +364,25 @@ l2_tc_kernel(const __grid_constant__ CUtensorMap mq_hi, const __grid_constant__ 
           for (int j = 0; j < 32; ++j) {
             const float u = fmaf(-2.f, v[j], xn[j]);
             if (cb + j < a.n) gm[cc * 32 + j] = fminf(gm[cc * 32 + j], u);
+          }
+        } else if (full) {
+          // full chunk: the pass mask first (no branch per entry), then the
+          // appends of this lane's few passing entries
+          uint32_t mk = 0;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            v[j] = fmaf(-2.f, v[j], __ldg(a.xnorm + cb + j));
+            mk |= uint32_t(v[j] <= bnd) << j;
+          }
+          if (mk != 0) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if ((mk >> j) & 1u) {
+                if (cnt < a.cap_s)
+                  seg[cnt] = (uint64_t(float_to_key(v[j] + qn)) << 32) | uint32_t(cb + j);
+                ++cnt;
+              }
+            }
           }
         } else {
 #pragma unroll
