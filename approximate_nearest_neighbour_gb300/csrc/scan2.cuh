@@ -102,12 +102,33 @@ ivfpq_scan2_kernel(const ScanParams p) {
       for (int t = 0; t < DS; ++t) r[t] = xs[t] - __ldg(cl + t);
     }
     const float* t1 = p.term1 + int64_t(l) * 256 * m + jj;
+    // m = 32: two table entries at a time with packed fp32x2 arithmetic
+    // (scan ms 16.05 -> 15.67 on 2e8 vectors; slower for m = 8, so not there)
+    constexpr bool PACKED = !PRE && MW == 8 && Sh::STEPS % 2 == 0;
+    float tv2[PACKED ? Sh::STEPS : 1];
+    if constexpr (PACKED) {
+#pragma unroll
+      for (int s = 0; s < Sh::STEPS; s += 2) {
+        unsigned long long acc = 0ull;
+#pragma unroll
+        for (int t = 0; t < DS; ++t) {
+          unsigned long long c2, r2, df;
+          asm("mov.b64 %0, {%1, %2};" : "=l"(c2) : "f"(cw[s][t]), "f"(cw[s + 1][t]));
+          asm("mov.b64 %0, {%1, %1};" : "=l"(r2) : "f"(r[t]));
+          asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(df) : "l"(r2), "l"(c2));
+          asm("fma.rn.f32x2 %0, %1, %1, %2;" : "=l"(acc) : "l"(df), "l"(acc));
+        }
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(tv2[s]), "=f"(tv2[s + 1]) : "l"(acc));
+      }
+    }
 #pragma unroll
     for (int s = 0; s < Sh::STEPS; ++s) {
       const int e = (s * NW + warp) * Sh::QQ + qq;
       float Tv = 0.f;
       if constexpr (PRE) {
         Tv = __ldg(t1 + e * m) + t3[s];
+      } else if constexpr (PACKED) {
+        Tv = tv2[s];
       } else {
 #pragma unroll
         for (int t = 0; t < DS; ++t) {
