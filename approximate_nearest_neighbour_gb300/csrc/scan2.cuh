@@ -15,8 +15,14 @@
 //  * the block's probe list (list id, length, first block) is staged in
 //    shared memory once, and each warp loads its first code block of list
 //    i+1 before the barrier that ends list i, so no list starts with a chain
-//    of dependent global loads; the next list is streamed into L2 with
-//    bulk prefetches while the current one is scanned;
+//    of dependent global loads; the list two ahead is streamed into L2 with
+//    bulk prefetches, and (m = 32) the centroid slice of the next table is
+//    loaded a list early;
+//  * for m < 32 a warp scores 16 / MW of its blocks per iteration; for
+//    m = 32 the tables are built with packed fp32x2 arithmetic;
+//  * optionally (ivfpq_set_precomputed, m <= 16) the table of a list is the
+//    stored list term plus the query's term, the list's exact coarse
+//    distance being added to its distances;
 //  * each warp keeps only its own KW best (WarpSelect with a KW-entry warp
 //    queue, KW < k allowed) and writes them out unmerged; the cross-chunk
 //    merge selects the k best of all warps' entries. That is exact unless a

@@ -1,6 +1,7 @@
 // k-selection over the per-row candidate segments of the filtered tensor-core
-// distance pass (gemm_tc.cu, l2_tc_filter): BlockSelect over the valid
-// entries of each row's segments. A row with an overflowed segment (more
+// distance pass (gemm_tc.cu, l2_tc_filter): WarpSelect over the valid entries
+// of each row's segments, one warp per row for k <= 256 and BlockSelect (four
+// warps and a shared-memory merge) for longer queues. A row with an overflowed segment (more
 // entries found than it holds) is selected instead over exact distances
 // sum_t (q_t - x_t)^2 to every column, computed here; the caller re-ranks the
 // winners in that exact form anyway.
