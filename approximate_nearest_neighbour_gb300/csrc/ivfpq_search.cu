@@ -32,13 +32,13 @@ IVFPQ_EXTERN_SCAN(16, 256)
 
 #define IVFPQ_EXTERN_SCAN2_1(MW, DS, KW, PRE) \
   extern template int launch_scan2<MW, DS, KW, PRE>(const ScanParams&, int64_t, cudaStream_t);
-#define IVFPQ_EXTERN_SCAN2(MW, DS)                                                        \
-  IVFPQ_EXTERN_SCAN2_1(MW, DS, 32, false) IVFPQ_EXTERN_SCAN2_1(MW, DS, 64, false)         \
-  IVFPQ_EXTERN_SCAN2_1(MW, DS, 32, true) IVFPQ_EXTERN_SCAN2_1(MW, DS, 64, true)
-IVFPQ_EXTERN_SCAN2_1(8, 3, 32, false)
-IVFPQ_EXTERN_SCAN2_1(8, 3, 64, false)
-IVFPQ_EXTERN_SCAN2_1(8, 4, 32, false)
-IVFPQ_EXTERN_SCAN2_1(8, 4, 64, false)
+#define IVFPQ_EXTERN_SCAN2_KW(MW, DS, PRE)                                                  \
+  IVFPQ_EXTERN_SCAN2_1(MW, DS, 32, PRE) IVFPQ_EXTERN_SCAN2_1(MW, DS, 64, PRE)               \
+  IVFPQ_EXTERN_SCAN2_1(MW, DS, 128, PRE) IVFPQ_EXTERN_SCAN2_1(MW, DS, 256, PRE)
+#define IVFPQ_EXTERN_SCAN2(MW, DS) \
+  IVFPQ_EXTERN_SCAN2_KW(MW, DS, false) IVFPQ_EXTERN_SCAN2_KW(MW, DS, true)
+IVFPQ_EXTERN_SCAN2_KW(8, 3, false)
+IVFPQ_EXTERN_SCAN2_KW(8, 4, false)
 IVFPQ_EXTERN_SCAN2(4, 8)
 IVFPQ_EXTERN_SCAN2(4, 4)
 IVFPQ_EXTERN_SCAN2(2, 12)
@@ -71,7 +71,7 @@ int try_scan2_kw(const ScanParams& p, int64_t nq, cudaStream_t s, int* launched)
 
 bool scan2_shape(const ScanParams& p) {
   const int key = p.m * 100 + p.dsub;
-  return p.lut_type == IVFPQ_LUT_FP32 && p.m * p.dsub == p.d && p.k <= 256 &&
+  return p.lut_type == IVFPQ_LUT_FP32 && p.m * p.dsub == p.d && p.k <= IVFPQ_MAX_K &&
          (key == 3203 || key == 3204 || key == 1608 || key == 1604 || key == 812 || key == 808);
 }
 
@@ -227,8 +227,12 @@ int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int npro
   IVFPQ_TRY(ws.alloc(&p.pidx, np));
   record(ix, 2, s);
   int launched = 0;
-  if (kw == 32) IVFPQ_TRY(try_scan2_kw<32>(p, nq, s, &launched));
-  else IVFPQ_TRY(try_scan2_kw<64>(p, nq, s, &launched));
+  switch (kw) {
+    case 32: IVFPQ_TRY(try_scan2_kw<32>(p, nq, s, &launched)); break;
+    case 64: IVFPQ_TRY(try_scan2_kw<64>(p, nq, s, &launched)); break;
+    case 128: IVFPQ_TRY(try_scan2_kw<128>(p, nq, s, &launched)); break;
+    default: IVFPQ_TRY(try_scan2_kw<256>(p, nq, s, &launched)); break;
+  }
   IVFPQ_REQUIRE(launched, "scan: no register-codebook kernel for m=%d d/m=%d", p.m, p.dsub);
   mix->last_scan_kernel.store("ivfpq_scan2_kernel");
   record(ix, 3, s);

@@ -215,7 +215,7 @@ ivfpq_scan2_kernel(const ScanParams p) {
   // (16 / MW measured faster than 8 / MW: scan ms 24.9 -> 23.9 for m = 8,
   // d/m = 12 and 12.5 -> 12.1 for m = 16, d/m = 8, although those two spill a
   // few bytes in the rarely taken merge path)
-  constexpr int R = MW >= 8 ? 1 : 16 / MW;
+  constexpr int R = MW >= 8 ? 1 : (KW >= 128 ? 8 : 16) / MW;  // longer queues: fewer registers
   uint32_t c0[R][MW], c1[R][MW];
   auto load_group = [&](const uint8_t* lc, int b, int nb, uint32_t (&c)[R][MW]) {
 #pragma unroll
@@ -277,9 +277,10 @@ ivfpq_scan2_kernel(const ScanParams p) {
 // two table buffers and the staged probe list
 inline size_t scan2_smem_bytes() { return size_t(2) * kGroupWords * 4 + kScan2MaxLists * 20; }
 
-// Warp-queue length for a result of k <= 256: each warp's share of the k
-// best is about k / 16, so 32 entries (64 for k > 128) leave a wide margin.
-inline int scan2_kw(int k) { return k <= 128 ? 32 : 64; }
+// Warp-queue length: each warp's share of the k best is about k / 16 (with a
+// binomial spread of about sqrt(k / 16)), so these leave a wide margin; a
+// query whose share overflowed anyway is repaired by the caller.
+inline int scan2_kw(int k) { return k <= 128 ? 32 : k <= 256 ? 64 : k <= 1024 ? 128 : 256; }
 
 template <int MW, int DS, int KW, bool PRE>
 int launch_scan2(const ScanParams& p, int64_t nq, cudaStream_t s) {

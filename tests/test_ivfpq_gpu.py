@@ -187,7 +187,8 @@ def test_preassigned_probes_with_repeats(B):
     assert np.all(np.abs(g - od) <= tol(od))
 
 
-@pytest.mark.parametrize("k,blocks", [(100, (0, 16, 32)), (200, (0, 16, 32, 48)), (40, (16, 48))])
+@pytest.mark.parametrize("k,blocks", [(100, (0, 16, 32)), (200, (0, 16, 32, 48)), (40, (16, 48)),
+                                      (1000, (0, 16, 32, 48, 64)), (2000, (0, 16, 32))])
 def test_results_concentrated_in_one_warp_are_repaired(B, k, blocks):
     """The list scan's per-warp queues are shorter than k (each warp of the
     register-codebook kernel takes code blocks b = w mod 16 of every list).
