@@ -15,7 +15,9 @@
  *    packed. `stream` is a cudaStream_t (NULL = the legacy default stream).
  *  - Calls enqueue work on `stream` and return without synchronizing, except
  *    ivfpq_add, which synchronizes `stream` once (it needs the new list sizes
- *    on the host to size the list storage).
+ *    on the host to size the list storage), ivfpq_device_check,
+ *    ivfpq_set_precomputed and the training calls (kmeans_lloyd, pq_train),
+ *    which return host results.
  *  - Argument errors are detected on the host before any work is enqueued; in
  *    that case nothing is written and IVFPQ_ERR_INVALID_ARG (or
  *    IVFPQ_ERR_UNSUPPORTED) is returned. CUDA errors return IVFPQ_ERR_CUDA,
@@ -195,7 +197,8 @@ int ivfpq_uses_precomputed(const ivfpq_index* index);
 
 /* ivfpq_last_scan_kernel -- name of the list-scan kernel family that the
  * most recent search of this index launched ("ivfpq_scan2_kernel": codebook
- * in registers, double-buffered fp32 tables; "ivfpq_scan_kernel": the general
+ * in registers, double-buffered fp32 tables, used for fp32 tables with (m,
+ * d/m) in {(32,3), (32,4), (16,8), (16,4), (8,12), (8,8)}; "ivfpq_scan_kernel": the general
  * kernel), or NULL before the first search; a measurement aid. */
 const char* ivfpq_last_scan_kernel(const ivfpq_index* index);
 
