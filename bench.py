@@ -486,7 +486,8 @@ def run_flat_reference(args):
     b = flat_cpu_baseline(db, q, target_s=max(1.0, 10.0 / max(args.steps, 1)))
     emit({"impl": "reference", "metric": f"flat k-NN queries/s (k={K})", "value": b["value"],
           "unit": "queries/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-          "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+          # the step's queries at the sample's rate
+          "ms_per_step": 1e3 * q.shape[0] / b["value"], "higher_is_better": True, "scaling": "weak",
           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
           "config": flat_config(args, db.shape[0], q.shape[0], db.shape[1]), "cpu_baseline": b,
           "e2e": {"value": b["value"], "unit": "queries/s", "h2d_bytes_per_step": 0,
