@@ -45,6 +45,12 @@ int select_rows(const float* vals, int64_t rows, int64_t cols, int k, int64_t ch
 int select_pairs(const uint32_t* keys, const uint32_t* idx, int64_t rows, int64_t len, int k,
                  int64_t chunks, int64_t chunk_len, const SelectOut& out, cudaStream_t s);
 
+// The k smallest of each row's `runs` runs of kw (key, index) pairs, each run
+// sorted ascending (rows of runs * kw entries): a bitonic merge tree in shared
+// memory (the pair selection when runs * kw exceeds 8,192).
+int merge_sorted_runs(const uint32_t* pk, const uint32_t* pi, int64_t rows, int runs, int kw, int k,
+                      const SelectOut& out, cudaStream_t s);
+
 // Two-level selection over long rows when there are few rows: a first pass
 // per column chunk into workspace, then a pass over the chunk winners.
 int kselect_device(const float* vals, int64_t rows, int64_t cols, int k, const SelectOut& out,

@@ -11,7 +11,6 @@
 
 #include "internal.h"
 #include "scan2.cuh"
-#include "select_inst.cuh"
 
 namespace ivfpq {
 
@@ -131,52 +130,6 @@ __global__ void warp_queue_check_kernel(const uint32_t* __restrict__ pkeys, int6
   flags[q] = f;
 }
 
-// The k smallest of a row's `runs` sorted runs of kw (key, slot) pairs
-// (ascending, sentinel-padded), by a tree of bitonic merges in shared memory
-// (each merge: the mirror comparison of two sorted runs, then half-cleaners):
-// one block per row, total = runs * kw rounded up to a power of two.
-__global__ void merge_runs_kernel(const uint32_t* __restrict__ pk, const uint32_t* __restrict__ pi,
-                                  int runs, int kw, int total, int k, OutWriter out) {
-  extern __shared__ uint32_t sm_runs[];
-  uint32_t* sk = sm_runs;
-  uint32_t* sv = sm_runs + total;
-  const int64_t row = blockIdx.x;
-  const int len = runs * kw;
-  for (int i = threadIdx.x; i < total; i += blockDim.x) {
-    const bool ok = i < len;
-    sk[i] = ok ? pk[row * len + i] : kSentinelKey;
-    sv[i] = ok ? pi[row * len + i] : kSentinelIdx;
-  }
-  __syncthreads();
-  auto cx = [&](int a, int b) {
-    const uint32_t ka = sk[a], kb = sk[b];
-    if (kb < ka) {
-      const uint32_t va = sv[a];
-      sk[a] = kb;
-      sk[b] = ka;
-      sv[a] = sv[b];
-      sv[b] = va;
-    }
-  };
-  for (int w = kw; w < total; w *= 2) {
-    for (int c = threadIdx.x; c < total / 2; c += blockDim.x) {
-      const int pair = c / w, t = c - pair * w;
-      cx(pair * 2 * w + t, pair * 2 * w + 2 * w - 1 - t);
-    }
-    __syncthreads();
-    for (int st = w / 2; st >= 1; st /= 2) {
-      for (int c = threadIdx.x; c < total / 2; c += blockDim.x) {
-        const int blk = c / st;
-        const int a = blk * 2 * st + (c - blk * st);
-        cx(a, a + st);
-      }
-      __syncthreads();
-    }
-  }
-  for (int i = threadIdx.x; i < k; i += blockDim.x)
-    out.write(row, 0, i, i < total ? sk[i] : kSentinelKey, i < total ? sv[i] : kSentinelIdx);
-}
-
 const size_t kMaxEventSets = 4096;
 
 // Starts a new event set for this search (profiling only).
@@ -283,19 +236,7 @@ int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int npro
   IVFPQ_REQUIRE(launched, "scan: no register-codebook kernel for m=%d d/m=%d", p.m, p.dsub);
   mix->last_scan_kernel.store("ivfpq_scan2_kernel");
   record(ix, 3, s);
-  const int64_t len = int64_t(groups) * kw;
-  int total = kw;
-  while (total < len) total *= 2;
-  if (total <= 8192) {
-    // the warp queues are sorted runs: merge them
-    const size_t smem = size_t(total) * 8;
-    if (smem > 48 * 1024) IVFPQ_TRY(set_dynamic_smem(merge_runs_kernel, smem));
-    merge_runs_kernel<<<unsigned(nq), 256, smem, s>>>(p.pkeys, p.pidx, groups, kw, total, k,
-                                                      OutWriter{o, k, 1});
-    IVFPQ_LAUNCHED_K(merge_runs_kernel, smem, 256);
-  } else {
-    IVFPQ_TRY(select_pairs(p.pkeys, p.pidx, nq, len, k, 1, len, o, s));
-  }
+  IVFPQ_TRY(merge_sorted_runs(p.pkeys, p.pidx, nq, groups, kw, k, o, s));
   if (kw < k) {
     // repair the queries whose merged result a short queue may have cut
     int* flags = nullptr;

@@ -83,6 +83,70 @@ int select_rows(const float* vals, int64_t rows, int64_t cols, int k, int64_t ch
   return IVFPQ_ERR_INVALID_ARG;
 }
 
+namespace {
+// The k smallest of a row's `runs` sorted runs of kw (key, index) pairs
+// (ascending, sentinel-padded), by a tree of bitonic merges in shared memory
+// (each merge: the mirror comparison of two sorted runs, then half-cleaners):
+// one block per row, total = runs * kw rounded up to a power of two.
+__global__ void merge_runs_kernel(const uint32_t* __restrict__ pk, const uint32_t* __restrict__ pi,
+                                  int runs, int kw, int total, int k, OutWriter out) {
+  extern __shared__ uint32_t sm_runs[];
+  uint32_t* sk = sm_runs;
+  uint32_t* sv = sm_runs + total;
+  const int64_t row = blockIdx.x;
+  const int len = runs * kw;
+  for (int i = threadIdx.x; i < total; i += blockDim.x) {
+    const bool ok = i < len;
+    sk[i] = ok ? pk[row * len + i] : kSentinelKey;
+    sv[i] = ok ? pi[row * len + i] : kSentinelIdx;
+  }
+  __syncthreads();
+  auto cx = [&](int a, int b) {
+    const uint32_t ka = sk[a], kb = sk[b];
+    if (kb < ka) {
+      const uint32_t va = sv[a];
+      sk[a] = kb;
+      sk[b] = ka;
+      sv[a] = sv[b];
+      sv[b] = va;
+    }
+  };
+  for (int w = kw; w < total; w *= 2) {
+    for (int c = threadIdx.x; c < total / 2; c += blockDim.x) {
+      const int pair = c / w, t = c - pair * w;
+      cx(pair * 2 * w + t, pair * 2 * w + 2 * w - 1 - t);
+    }
+    __syncthreads();
+    for (int st = w / 2; st >= 1; st /= 2) {
+      for (int c = threadIdx.x; c < total / 2; c += blockDim.x) {
+        const int blk = c / st;
+        const int a = blk * 2 * st + (c - blk * st);
+        cx(a, a + st);
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < k; i += blockDim.x)
+    out.write(row, 0, i, i < total ? sk[i] : kSentinelKey, i < total ? sv[i] : kSentinelIdx);
+}
+
+}  // namespace
+
+int merge_sorted_runs(const uint32_t* pk, const uint32_t* pi, int64_t rows, int runs, int kw, int k,
+                      const SelectOut& out, cudaStream_t s) {
+  if (rows == 0) return IVFPQ_OK;
+  const int64_t len = int64_t(runs) * kw;
+  int64_t total = kw;
+  while (total < len) total *= 2;
+  if (total > 8192) return select_pairs(pk, pi, rows, len, k, 1, len, out, s);
+  const size_t smem = size_t(total) * 8;
+  if (smem > 48 * 1024) IVFPQ_TRY(set_dynamic_smem(merge_runs_kernel, smem));
+  merge_runs_kernel<<<unsigned(rows), 256, smem, s>>>(pk, pi, runs, kw, int(total), k,
+                                                     OutWriter{out, k, 1});
+  IVFPQ_LAUNCHED_K(merge_runs_kernel, smem, 256);
+  return IVFPQ_OK;
+}
+
 int select_pairs(const uint32_t* keys, const uint32_t* idx, int64_t rows, int64_t len, int k,
                  int64_t chunks, int64_t chunk_len, const SelectOut& out, cudaStream_t s) {
   if (rows == 0) return IVFPQ_OK;

@@ -50,7 +50,7 @@ int select_long(const uint64_t* cand, const int* scnt, int nseg, int cap_s, int6
   part.kind = OutKind::Partial;
   part.pkeys = tk;
   part.pidx = ti;
-  IVFPQ_TRY(select_pairs(pk, pi, rows, 16 * KW, k, 1, 16 * KW, part, s));
+  IVFPQ_TRY(merge_sorted_runs(pk, pi, rows, 16, KW, k, part, s));
   IVFPQ_TRY(launch_cand_check<KW>(pk, tk, over, rows, k, flags, s));
   cand_emit_kernel<<<unsigned(std::min<int64_t>(ceil_div(rows * k, 256), 65535 * 8)), 256, 0,
                      s>>>(tk, ti, rows, k, OutWriter{out, k, 1});
