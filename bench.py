@@ -53,14 +53,17 @@ def parse():
     p.add_argument("--nlist", type=int, default=None, help="list count override (development)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--workload", default="large", choices=sorted(WORKLOADS),
-                   help="large (default, the headline), mid, billion, or flat (exact k-NN)")
+                   help="large (default, the headline), mid, billion, flat (exact k-NN) "
+                        "or kselect (stand-alone k-selection)")
     p.add_argument("--k", type=int, default=None, help="k override")
     return p.parse_args()
 
 
 # workload -> (shape, nprobe, k); "large" is the configuration the scan target is quoted on
 WORKLOADS = {"large": (S.IVFPQ_LARGE, 64, 100), "mid": (S.IVFPQ_MID, 64, 100),
-             "billion": (S.IVFPQ_BILLION, 128, 100), "flat": (S.FLAT_1M, 0, 100)}
+             "billion": (S.IVFPQ_BILLION, 128, 100), "flat": (S.FLAT_1M, 0, 100),
+             "kselect": (None, 0, 100)}
+KSELECT_ROWS, KSELECT_COLS = 10_000, 65_536  # 2.6 GB of fp32 rows, above L2
 WORKLOAD = S.IVFPQ_LARGE
 NPROBE, K = 64, 100
 
@@ -494,13 +497,115 @@ def run_flat_reference(args):
                   "d2h_bytes_per_step": 0}})
 
 
+# ---------------------------------------------------------------------------
+# stand-alone row-wise k-selection: 10,000 rows x 65,536 fp32 values
+def run_kselect(args):
+    import numpy as np
+    import torch
+    from approximate_nearest_neighbour_gb300 import binding as B
+
+    world, rank, local = dist_env()
+    rows, cols = args.nq or KSELECT_ROWS, args.n or KSELECT_COLS
+    x = S.random_rows(rows, cols, seed=20260)
+    if args.impl == "reference":
+        if rank == 0:
+            run_kselect_reference(args, x)
+        return
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    vals = torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(dev)
+    out_v = torch.empty((rows, K), dtype=torch.float32, device=dev)
+    out_i = torch.empty((rows, K), dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        B.kselect(vals, K, out_v, out_i)
+    torch.cuda.synchronize()
+    clocks = Clocks(local)
+    launches0 = B.kernel_launches()
+    clocks.start()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        B.kselect(vals, K, out_v, out_i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    launches = B.kernel_launches() - launches0
+    call_s = e0.elapsed_time(e1) / 1e3 / args.steps
+    # end to end: host rows in, host results out
+    xh = torch.from_numpy(np.ascontiguousarray(x, np.float32)).pin_memory()
+    hv = torch.empty((rows, K), dtype=torch.float32).pin_memory()
+    hi = torch.empty((rows, K), dtype=torch.int64).pin_memory()
+    buf = torch.empty_like(vals)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        buf.copy_(xh, non_blocking=True)
+        B.kselect(buf, K, out_v, out_i)
+        hv.copy_(out_v, non_blocking=True)
+        hi.copy_(out_i, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3 / args.steps
+    peak, kind = peaks()
+    nbytes = 4.0 * rows * cols
+    line = {"metric": f"kselect rows/s (k={K}, {cols} columns)", "value": rows / call_s,
+            "unit": "rows/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * call_s, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"kselect_{rows}x{cols}", "rows": rows, "cols": cols, "k": K,
+                       "l2": f"input {nbytes / 1e9:.2f} GB, above L2"},
+            "roofline": {"bound": "hbm", "kernel": "kselect (all kernels of one call)", "achieved": nbytes / call_s / 1e9,
+                         "peak": peak, "unit": "GB/s", "frac": nbytes / call_s / 1e9 / peak,
+                         "peak_source": f"{kind} hbm_gbs (copy)", "traffic": None,
+                         "algorithmic_bytes_per_call": nbytes},
+            "e2e": {"value": rows / e2e_s, "unit": "rows/s", "h2d_bytes_per_step": int(nbytes),
+                    "d2h_bytes_per_step": int(rows * K * 12)},
+            "gpu_launches": launches, "clocks": clk}
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = kselect_cpu_baseline(x)
+    emit(line)
+
+
+def kselect_cpu_baseline(x, target_s=10.0):
+    import oracle
+    threads = oracle.NTHREADS
+    m = min(x.shape[0], 2 * threads)
+    t0 = time.perf_counter()
+    oracle.kselect(x[:m], K)
+    dt = time.perf_counter() - t0
+    m = int(min(x.shape[0], max(m, target_s / max(dt, 1e-6) * m)))
+    t0 = time.perf_counter()
+    oracle.kselect(x[:m], K)
+    dt = time.perf_counter() - t0
+    return {"value": m / dt, "unit": "rows/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {m} of the {x.shape[0]} rows, {threads} threads, {dt:.1f} s"}
+
+
+def run_kselect_reference(args, x):
+    rows, cols = x.shape
+    b = kselect_cpu_baseline(x, target_s=max(1.0, 10.0 / max(args.steps, 1)))
+    emit({"impl": "reference", "metric": f"kselect rows/s (k={K}, {cols} columns)",
+          "value": b["value"], "unit": "rows/s", "n_gpus": args.gpus, "steps": args.steps,
+          "warmup": args.warmup, "ms_per_step": 1e3 * rows / b["value"],
+          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+          "data": "synthetic",
+          "config": {"workload": f"kselect_{rows}x{cols}", "rows": rows, "cols": cols, "k": K},
+          "cpu_baseline": b,
+          "e2e": {"value": b["value"], "unit": "rows/s", "h2d_bytes_per_step": 0,
+                  "d2h_bytes_per_step": 0}})
+
+
 def main():
     global WORKLOAD, NPROBE, K
     args = parse()
     WORKLOAD, NPROBE, K = WORKLOADS[args.workload]
     if args.k is not None:
         K = args.k
-    if args.workload == "flat":
+    if args.workload == "kselect":
+        run_kselect(args)
+    elif args.workload == "flat":
         if args.impl == "reference":
             run_flat_reference(args)
         else:

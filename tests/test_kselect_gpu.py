@@ -53,3 +53,17 @@ def test_kselect_unaligned_rows(B):
     gv, gi = B.kselect(full, 50)
     ov, oi = oracle.kselect(vals, 50)
     check_kselect(vals, 50, ov, oi, gv.cpu().numpy(), gi.cpu().numpy())
+
+
+@pytest.mark.parametrize("kind", ["normal", "ties", "equal", "sorted", "reverse", "inf"])
+@pytest.mark.parametrize("k,cols", [(1, 32768), (100, 33001), (1000, 32768), (2048, 40000)])
+def test_kselect_many_long_rows(B, kind, k, cols):
+    """Many long rows take the short-queue path: 16 warps per row with queues
+    of max(32, K/8), their merge, and the full-queue kernel again for the rows
+    a short queue may have cut. Sorted rows put every winner in one warp's
+    columns, ties and equal rows make every queue end at the k-th value, so
+    those rows go through the repair; an odd width takes the scalar loads."""
+    vals = S.random_rows(640, cols, seed=3 * k + cols, kind=kind)
+    gv, gi = _run(B, vals, k)
+    ov, oi = oracle.kselect(vals, k)
+    check_kselect(vals, k, ov, oi, gv, gi)
