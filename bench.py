@@ -179,9 +179,48 @@ def cpu_baseline(data, q, lut, target_s=12.0, max_queries=4096):
     oracle.ivfpq_search(q[:n], data.cent, data.cb, data.list_off, data.codes, data.ids,
                         NPROBE, K, lut_type)
     dt = time.perf_counter() - t0
+    one = min(16, q.shape[0])
+    t0 = time.perf_counter()
+    oracle.ivfpq_search(q[:one], data.cent, data.cb, data.list_off, data.codes, data.ids,
+                        NPROBE, K, lut_type, nthreads=1)
+    dt1 = time.perf_counter() - t0
     return {"value": n / dt, "unit": "queries/s", "cores": threads, "kind": "oracle",
             "sample": f"first {n} of the {q.shape[0]} step queries, full index, "
-                      f"{threads} threads, {dt:.1f} s"}
+                      f"{threads} threads, {dt:.1f} s",
+            "per_core": {"value": one / dt1, "unit": "queries/s",
+                         "sample": f"first {one} queries, 1 thread, {dt1:.2f} s"},
+            "cpu_model": cpu_model()}
+
+
+L2_BYTES = 129e6  # GB300 L2
+
+
+def l2_note(nbytes, what):
+    """Whether the step's input is larger than L2 (no flush between steps is
+    then needed) or would stay cached between steps."""
+    where = "larger than L2" if nbytes > L2_BYTES else "fits in L2: timed warm, no flush"
+    return f"{what} {nbytes / 1e9:.2f} GB, {where}"
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    import platform
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
 
 
 def emit(obj):
@@ -228,7 +267,7 @@ def config_dict(args, data):
     return {"workload": w.name if not scaled else f"{w.name}(N={n},nlist={nlist})", "n": n,
             "d": w.d, "nlist": nlist, "m": w.m, "nq_per_gpu": args.nq or w.nq, "nprobe": NPROBE, "k": K,
             "lut": args.lut, "parallelism": f"replicas x{args.gpus}",
-            "l2": f"inputs larger than L2 ({n * w.m / 1e9:.1f} GB of PQ codes)"}
+            "l2": l2_note(n * w.m, "PQ codes")}
 
 
 def run_ours(args):
@@ -375,8 +414,7 @@ def tf32_peak():
 def flat_config(args, n, nq, d):
     return {"workload": WORKLOAD.name if args.n is None else f"{WORKLOAD.name}(N={n})", "n": n,
             "d": d, "nq_per_gpu": nq, "k": K, "parallelism": f"replicas x{args.gpus}",
-            "l2": f"database {n * d * 4 / 1e9:.2f} GB fp32 + {2 * n * 128 * 4 / 1e9:.2f} GB "
-                  f"tensor-core operands, above L2"}
+            "l2": l2_note(n * d * 4 + 2 * n * 128 * 4, "fp32 database + tensor-core operands")}
 
 
 def run_flat(args):
@@ -476,9 +514,16 @@ def flat_cpu_baseline(db, q, target_s=10.0):
     t0 = time.perf_counter()
     oracle.flat_knn(db, q[:nsel], K)
     dt = time.perf_counter() - t0
+    one = min(4, q.shape[0])
+    t0 = time.perf_counter()
+    oracle.flat_knn(db, q[:one], K, nthreads=1)
+    dt1 = time.perf_counter() - t0
     return {"value": nsel / dt, "unit": "queries/s", "cores": threads, "kind": "oracle",
             "sample": f"first {nsel} of the {q.shape[0]} queries, full database, "
-                      f"{threads} threads, {dt:.1f} s"}
+                      f"{threads} threads, {dt:.1f} s",
+            "per_core": {"value": one / dt1, "unit": "queries/s",
+                         "sample": f"first {one} queries, 1 thread, {dt1:.2f} s"},
+            "cpu_model": cpu_model()}
 
 
 def run_flat_reference(args):
@@ -555,7 +600,7 @@ def run_kselect(args):
             "ms_per_step": 1e3 * call_s, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": f"kselect_{rows}x{cols}", "rows": rows, "cols": cols, "k": K,
-                       "l2": f"input {nbytes / 1e9:.2f} GB, above L2"},
+                       "l2": l2_note(nbytes, "fp32 input")},
             "roofline": {"bound": "hbm", "kernel": "kselect (all kernels of one call)", "achieved": nbytes / call_s / 1e9,
                          "peak": peak, "unit": "GB/s", "frac": nbytes / call_s / 1e9 / peak,
                          "peak_source": f"{kind} hbm_gbs (copy)", "traffic": None,
@@ -579,8 +624,15 @@ def kselect_cpu_baseline(x, target_s=10.0):
     t0 = time.perf_counter()
     oracle.kselect(x[:m], K)
     dt = time.perf_counter() - t0
+    one = min(16, x.shape[0])
+    t0 = time.perf_counter()
+    oracle.kselect(x[:one], K, nthreads=1)
+    dt1 = time.perf_counter() - t0
     return {"value": m / dt, "unit": "rows/s", "cores": threads, "kind": "oracle",
-            "sample": f"first {m} of the {x.shape[0]} rows, {threads} threads, {dt:.1f} s"}
+            "sample": f"first {m} of the {x.shape[0]} rows, {threads} threads, {dt:.1f} s",
+            "per_core": {"value": one / dt1, "unit": "rows/s",
+                         "sample": f"first {one} rows, 1 thread, {dt1:.2f} s"},
+            "cpu_model": cpu_model()}
 
 
 def run_kselect_reference(args, x):
