@@ -331,5 +331,35 @@ def test_pq_training_objective_decreases_and_encoding_is_nearest():
     assert abs(err - obj[-1]) <= 1e-9 * err
 
 
+def test_one_lloyd_pass_is_the_mean_of_the_nearest_points():
+    """Closed form of one Lloyd pass ([BSS] section 6: assignment, then
+    update): each codeword becomes the mean of the points whose nearest seed
+    it is (brute force, lowest index on ties), a seed nobody chose stays, and
+    the first objective is the sum of the squared distances to the nearest
+    seed."""
+    g = _rng(12)
+    m, dsub, n = 2, 3, 2000
+    x = g.standard_normal((n, m * dsub)).astype(np.float32)
+    init = g.choice(n, 256, replace=False)
+    # two seeds on the same point: the higher-indexed one stays empty
+    init[7] = init[3]
+    cb, obj = oracle.pq_train(x, m, 1, init)
+    x64 = x.astype(np.float64)
+    total = 0.0
+    for j in range(m):
+        sub = x64[:, j * dsub:(j + 1) * dsub]
+        seeds = sub[init]
+        dd = ssd.cdist(sub, seeds, "sqeuclidean")
+        a = dd.argmin(1)
+        total += dd[np.arange(n), a].sum()
+        for c in range(256):
+            pts = sub[a == c]
+            want = pts.mean(0) if len(pts) else seeds[c]
+            assert np.allclose(cb[j, c], want, rtol=1e-6, atol=1e-6), (j, c)
+        assert not (a == 7).any()
+        assert np.array_equal(cb[j, 7], x[init[7], j * dsub:(j + 1) * dsub])
+    assert abs(obj[0] - total) <= 1e-9 * total
+
+
 def test_recall_definition():
     assert oracle.recall_at_k(np.array([[1, 2, 3]]), np.array([[3, 2, 9]])) == pytest.approx(2 / 3)
