@@ -165,29 +165,36 @@ int select_pairs(const uint32_t* keys, const uint32_t* idx, int64_t rows, int64_
 
 namespace {
 
-// Long rows, first level: one block of 16 warps per row.
+// Long rows: one block of 16 warps per row.
 //  1. A bound: a 4096-bin histogram of the top 12 key bits of the row's first
 //     `sample` values (sample >= k). The bin holding the sample's k-th
 //     smallest key ends at theta; at least k values of the row are <= theta,
 //     so every value of the row's k smallest is <= theta as well.
-//  2. Each warp streams its columns (thread t of the block takes float4 t,
-//     t + 512, ... when the row is 16-byte aligned, single floats otherwise)
-//     into a KW-entry WarpSelect that only sees keys <= theta, and writes its
-//     sorted queue to pk/pi[row][warp].
-template <int KW>
+//  2. The warps stream the row (thread t of the block takes float4 t, t + 512,
+//     ... when the row is 16-byte aligned, single floats otherwise) and append
+//     every key <= theta with its column to a shared buffer of `cap` entries
+//     (one atomic per warp and value position).
+//  3. One bitonic sort of the buffer; its first k entries are the result.
+// There are at least k candidates (the sample's own). A row with more than
+// `cap` writes nothing and sets flags[row] = 1 for the full-queue kernel.
 __global__ void __launch_bounds__(512)
-row_short_kernel(const float* __restrict__ vals, int64_t cols, int64_t sample, int k,
-                 uint32_t* __restrict__ pk, uint32_t* __restrict__ pi) {
-  constexpr int T = ThreadQ<KW>::value;
+row_cand_kernel(const float* __restrict__ vals, int64_t cols, int64_t sample, int k, int cap,
+                OutWriter out, int* __restrict__ flags) {
   constexpr int kBins = 4096, kShift = 20, kPer = kBins / 512;
-  __shared__ uint32_t hist[kBins];
+  extern __shared__ uint32_t sm_cand[];
+  uint32_t* hist = sm_cand;
+  uint32_t* ck = sm_cand + kBins;
+  uint32_t* ci = ck + cap;
   __shared__ uint32_t part[16];
-  __shared__ uint32_t theta_s;
+  __shared__ uint32_t theta_s, count_s;
   const int64_t row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* rp = vals + row * cols;
   for (int b = threadIdx.x; b < kBins; b += 512) hist[b] = 0;
-  if (threadIdx.x == 0) theta_s = kSentinelKey;
+  if (threadIdx.x == 0) {
+    theta_s = kSentinelKey;
+    count_s = 0;
+  }
   __syncthreads();
   for (int64_t c = threadIdx.x; c < sample; c += 512)
     atomicAdd(&hist[float_to_key(__ldg(rp + c)) >> kShift], 1u);
@@ -225,13 +232,25 @@ row_short_kernel(const float* __restrict__ vals, int64_t cols, int64_t sample, i
   }
   __syncthreads();
   const uint32_t theta = theta_s;
-  WarpSelect<KW, T> ws;
-  ws.init(lane);
+  const uint32_t below = (1u << lane) - 1u;
+  // append the lanes' keys <= theta: the warp's leader reserves the slots
+  auto append = [&](bool pass, uint32_t key, uint32_t col) {
+    const uint32_t bal = __ballot_sync(kFullMask, pass);
+    if (bal == 0u) return;
+    const int leader = __ffs(bal) - 1;
+    uint32_t base = 0;
+    if (lane == leader) base = atomicAdd(&count_s, uint32_t(__popc(bal)));
+    base = __shfl_sync(kFullMask, base, leader);
+    const uint32_t pos = base + uint32_t(__popc(bal & below));
+    if (pass && pos < uint32_t(cap)) {
+      ck[pos] = key;
+      ci[pos] = col;
+    }
+  };
   const bool vec = (cols & 3) == 0 && (reinterpret_cast<uintptr_t>(vals) & 15) == 0;
   if (vec) {
-    // Four float4 loads in flight per thread (a rotating buffer), one vote per
-    // float4 against theta, and one insert site in the loop so that the
-    // inlined queue merge is not copied.
+    // four float4 loads in flight per thread (a rotating buffer); one vote
+    // per float4 skips the appends when no lane holds a key <= theta
     const float4* p4 = reinterpret_cast<const float4*>(rp);
     const int64_t n4 = cols >> 2;
     auto ld = [&](int64_t i4) {
@@ -253,11 +272,11 @@ row_short_kernel(const float* __restrict__ vals, int64_t cols, int64_t sample, i
       const uint32_t k3 = ok ? float_to_key(x.w) : kSentinelKey;
       const uint32_t lo = min(min(k0, k1), min(k2, k3));
       if (__any_sync(kFullMask, ok && lo <= theta)) {
-#pragma unroll 1
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t key = e == 0 ? k0 : (e == 1 ? k1 : (e == 2 ? k2 : k3));
-          ws.add(ok && key <= theta ? key : kSentinelKey, uint32_t(i4 * 4 + e));
-        }
+        const uint32_t c = uint32_t(i4 * 4);
+        append(ok && k0 <= theta, k0, c);
+        append(ok && k1 <= theta, k1, c + 1);
+        append(ok && k2 <= theta, k2, c + 2);
+        append(ok && k3 <= theta, k3, c + 3);
       }
     }
   } else {
@@ -265,74 +284,62 @@ row_short_kernel(const float* __restrict__ vals, int64_t cols, int64_t sample, i
     for (int64_t c = threadIdx.x; c - threadIdx.x < cols; c += 512) {
       const bool ok = c < cols;
       const uint32_t key = ok ? float_to_key(__ldcs(rp + c)) : kSentinelKey;
-      if (__any_sync(kFullMask, ok && key <= theta))
-        ws.add(ok && key <= theta ? key : kSentinelKey, uint32_t(c));
+      append(ok && key <= theta, key, uint32_t(c));
     }
   }
-  ws.finalize();
-  const int64_t o = (row * 16 + warp) * KW;
-#pragma unroll
-  for (int r = 0; r < KW / 32; ++r) {
-    pk[o + 32 * r + lane] = ws.wk[r];
-    pi[o + 32 * r + lane] = ws.wv[r];
+  __syncthreads();
+  const uint32_t cnt = count_s;
+  if (cnt > uint32_t(cap)) {  // block-uniform
+    if (threadIdx.x == 0) flags[row] = 1;
+    return;
   }
+  if (threadIdx.x == 0) flags[row] = 0;
+  uint32_t P = 1;
+  while (P < cnt) P <<= 1;
+  for (uint32_t i = cnt + threadIdx.x; i < P; i += 512) {
+    ck[i] = kSentinelKey;
+    ci[i] = kSentinelIdx;
+  }
+  __syncthreads();
+  for (uint32_t size = 2; size <= P; size <<= 1) {
+    for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
+      for (uint32_t t = threadIdx.x; t < P / 2; t += 512) {
+        const uint32_t a = 2 * t - (t & (stride - 1));
+        const uint32_t b = a + stride;
+        const uint32_t ka = ck[a], kb = ck[b];
+        if ((ka > kb) == ((a & size) == 0)) {
+          const uint32_t va = ci[a];
+          ck[a] = kb;
+          ck[b] = ka;
+          ci[a] = ci[b];
+          ci[b] = va;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < k; i += 512)
+    out.write(row, 0, i, uint32_t(i) < cnt ? ck[i] : kSentinelKey,
+              uint32_t(i) < cnt ? ci[i] : kSentinelIdx);
 }
 
-// flags[row] = 1 if the merged k best (tk, ascending) may miss an entry that
-// a full short queue dropped (its last key not above the k-th).
-template <int KW>
-__global__ void row_short_check_kernel(const uint32_t* __restrict__ pk,
-                                       const uint32_t* __restrict__ tk, int64_t rows, int k,
-                                       int* __restrict__ flags) {
-  const int64_t r = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (r >= rows) return;
-  const uint32_t theta = tk[r * k + k - 1];
-  int f = 0;
-  for (int w = 0; w < 16; ++w) {
-    const uint32_t last = pk[(r * 16 + w) * KW + KW - 1];
-    f |= last != kSentinelKey && last <= theta;
-  }
-  flags[r] = f;
-}
-
-// Ascending (key, index) rows [rows][k] through the output writer.
-__global__ void row_emit_kernel(const uint32_t* __restrict__ tk, const uint32_t* __restrict__ ti,
-                                int64_t rows, int k, OutWriter out) {
-  for (int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; t < rows * k;
-       t += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = t / k;
-    out.write(r, 0, int(t - r * k), tk[t], ti[t]);
-  }
-}
-
-// Selection over long rows with short queues: the first level above, the
-// sorted-run merge of the 16 queues, and the full-length row kernel again for
-// the rows a short queue may have cut (a warp's share of the k best is about
-// k / 16, far below KW = max(32, K / 8)).
-template <int KW>
-int select_rows_short(const float* vals, int64_t rows, int64_t cols, int k, const SelectOut& out,
-                      cudaStream_t s) {
+// Selection over many long rows by a bound and a candidate buffer (above);
+// the full-length row kernel redoes the rows whose buffer overflowed.
+int select_rows_cand(const float* vals, int64_t rows, int64_t cols, int k, const SelectOut& out,
+                     cudaStream_t s) {
+  constexpr int kMaxCap = 16384;
+  const int64_t sample = std::min<int64_t>(cols / 2, std::max<int64_t>(8192, 32 * int64_t(k)));
+  const int64_t expect = ceil_div(int64_t(k) * cols, sample);
+  int cap = 1024;
+  while (cap < 2 * expect + 512 && cap < kMaxCap) cap *= 2;
+  const size_t smem = (size_t(4096) + 2 * size_t(cap)) * 4;
+  IVFPQ_TRY(set_dynamic_smem(row_cand_kernel, smem));
   Workspace ws(s);
-  uint32_t *pk = nullptr, *pi = nullptr, *tk = nullptr, *ti = nullptr;
   int* flags = nullptr;
-  IVFPQ_TRY(ws.alloc(&pk, size_t(rows) * 16 * KW));
-  IVFPQ_TRY(ws.alloc(&pi, size_t(rows) * 16 * KW));
-  IVFPQ_TRY(ws.alloc(&tk, size_t(rows) * k));
-  IVFPQ_TRY(ws.alloc(&ti, size_t(rows) * k));
   IVFPQ_TRY(ws.alloc(&flags, size_t(rows)));
-  const int64_t sample = std::min<int64_t>(cols, std::max<int64_t>(8192, 16 * int64_t(k)));
-  row_short_kernel<KW><<<unsigned(rows), 512, 0, s>>>(vals, cols, sample, k, pk, pi);
-  IVFPQ_LAUNCHED();
-  SelectOut part;
-  part.kind = OutKind::Partial;
-  part.pkeys = tk;
-  part.pidx = ti;
-  IVFPQ_TRY(merge_sorted_runs(pk, pi, rows, 16, KW, k, part, s));
-  row_short_check_kernel<KW><<<unsigned(ceil_div(rows, 256)), 256, 0, s>>>(pk, tk, rows, k, flags);
-  IVFPQ_LAUNCHED();
-  row_emit_kernel<<<unsigned(std::min<int64_t>(ceil_div(rows * k, 256), 65535 * 8)), 256, 0, s>>>(
-      tk, ti, rows, k, OutWriter{out, k, 1});
-  IVFPQ_LAUNCHED();
+  row_cand_kernel<<<unsigned(rows), 512, smem, s>>>(vals, cols, sample, k, cap,
+                                                    OutWriter{out, k, 1}, flags);
+  IVFPQ_LAUNCHED_K(row_cand_kernel, smem, 512);
   SelectOut ro = out;
   ro.row_mask = flags;
   return select_rows(vals, rows, cols, k, 1, cols, ro, s);
@@ -343,20 +350,12 @@ int select_rows_short(const float* vals, int64_t rows, int64_t cols, int k, cons
 int kselect_device(const float* vals, int64_t rows, int64_t cols, int k, const SelectOut& out,
                    cudaStream_t s) {
   if (rows == 0) return IVFPQ_OK;
-  // Many long rows: short warp queues. Otherwise one pass when there are
+  // Many long rows: a bound and a candidate buffer. Otherwise one pass when there are
   // enough rows to fill the GPU, else each row is cut into chunks whose
   // winners (k per chunk) are selected again.
   if (rows >= 4 * int64_t(num_sms()) && cols >= 32768 && cols < (int64_t(1) << 31) &&
       out.kind != OutKind::Partial && !out.row_mask) {
-    switch (queue_len(k)) {
-      case 32:
-      case 64:
-      case 128:
-      case 256: return select_rows_short<32>(vals, rows, cols, k, out, s);
-      case 512: return select_rows_short<64>(vals, rows, cols, k, out, s);
-      case 1024: return select_rows_short<128>(vals, rows, cols, k, out, s);
-      case 2048: return select_rows_short<256>(vals, rows, cols, k, out, s);
-    }
+    return select_rows_cand(vals, rows, cols, k, out, s);
   }
   const int64_t target_blocks = 4 * int64_t(num_sms());
   const int64_t min_chunk = std::max<int64_t>(16384, 8 * int64_t(queue_len(k)));
