@@ -223,7 +223,11 @@ int flat_knn(const float* db, int64_t n, int d, const float* queries, int64_t nq
  * kselect -- the k smallest values of each row with their column index.
  * Source: WarpSelect ("Billion-scale similarity search with GPUs", section 4,
  * Algorithm 3) with BlockSelect (several warps, queues merged in shared memory)
- * for long rows.
+ * for long rows. With at least 4 rows per SM and at least 32768 columns, a
+ * row's k smallest are instead taken from the values at or below a bound read
+ * off a histogram of the row's first values (a shared buffer, one sort); a
+ * row with too many such values (many equal values) is redone by the queues.
+ * Results are the same either way; equal values may come in any order.
  *  vals      device fp32 [rows, cols]; +-inf allowed, NaN not supported
  *  k         1 .. IVFPQ_MAX_K;  cols < 2^32 - 1
  *  out_vals  device fp32 [rows, k];  out_idx  device int64 [rows, k]
