@@ -550,11 +550,12 @@ def run_kselect(args):
     from approximate_nearest_neighbour_gb300 import binding as B
 
     world, rank, local = dist_env()
+    if args.impl == "reference" and rank != 0:
+        return
     rows, cols = args.nq or KSELECT_ROWS, args.n or KSELECT_COLS
     x = S.random_rows(rows, cols, seed=20260)
     if args.impl == "reference":
-        if rank == 0:
-            run_kselect_reference(args, x)
+        run_kselect_reference(args, x)
         return
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
