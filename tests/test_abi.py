@@ -63,6 +63,41 @@ def test_host_side_argument_errors(lib):
     assert lib.ivfpq_status_string(-3) == b"IVFPQ_ERR_OOM"
 
 
+def test_host_side_argument_errors_of_the_other_entries(lib):
+    """Index preparation, sharded merge, graph and no-alloc selection reject
+    bad sizes and null pointers on the host, with a message."""
+    from approximate_nearest_neighbour_gb300 import binding as B
+    vp = C.c_void_p(16)
+    bad = B.IVFPQ_ERR_INVALID_ARG
+    cases = [
+        # k-means: k > n, k < 1, bad d, null seeds
+        lambda: lib.kmeans_lloyd(vp, 10, 4, 11, 1, vp, vp, vp, vp, None),
+        lambda: lib.kmeans_lloyd(vp, 10, 4, 0, 1, vp, vp, vp, vp, None),
+        lambda: lib.kmeans_lloyd(vp, 10, 0, 3, 1, vp, vp, vp, vp, None),
+        lambda: lib.kmeans_lloyd(vp, 10, 4, 3, 1, None, vp, vp, vp, None),
+        # PQ training: d not a multiple of m, fewer points than codewords
+        lambda: lib.pq_train(vp, 1000, 10, 4, 1, vp, vp, vp, None),
+        lambda: lib.pq_train(vp, 100, 16, 4, 1, vp, vp, vp, None),
+        # encoder / graph / preassigned search without an index
+        lambda: lib.ivfpq_encode(None, vp, 5, vp, vp, None),
+        lambda: lib.ivfpq_knn_graph(None, vp, vp, 5, 1, 1, vp, vp, None),
+        lambda: lib.ivfpq_search_preassigned(None, vp, 1, 1, vp, 1, vp, vp, None),
+        lambda: lib.ivfpq_search_probes(None, vp, 1, 1, vp, vp, None),
+        lambda: lib.ivfpq_set_precomputed(None, 0),
+        # merge: k beyond the limit, no shards, null inputs
+        lambda: lib.knn_merge(vp, vp, 4, 2, 10, 2049, vp, vp, None),
+        lambda: lib.knn_merge(vp, vp, 4, 0, 10, 5, vp, vp, None),
+        lambda: lib.knn_merge(None, vp, 4, 2, 10, 5, vp, vp, None),
+        # no-alloc selection: k and the fixed workspace limit
+        lambda: lib.kselect_noalloc(vp, 4, 10, 0, vp, vp, None),
+        lambda: lib.kselect_noalloc(vp, 1 << 20, 1 << 20, 2048, vp, vp, None),
+    ]
+    for i, call in enumerate(cases):
+        rc = call()
+        assert rc == bad, (i, rc, lib.ivfpq_last_error())
+        assert lib.ivfpq_last_error(), i
+
+
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     from approximate_nearest_neighbour_gb300 import binding as B
     monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "absent.so"))
