@@ -129,6 +129,32 @@ def _need(t, dtype, name, ndim=None, device=True):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _out(t, shape, dtype, name, device):
+    """A caller-given output checked against the shape the call writes
+    (the library trusts its pointers), or a new tensor."""
+    torch = _torch()
+    shape = tuple(int(v) for v in shape)
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != shape:
+        raise ValueError(f"{name} must have shape {shape}, got {tuple(t.shape)}")
+    if t.device != torch.device(device):
+        raise ValueError(f"{name} must be on {device} (the inputs' device), got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _same_device(what, *tensors):
+    devs = {t.device for t in tensors if t is not None}
+    if len(devs) > 1:
+        raise ValueError(f"{what}: tensors on several devices {sorted(map(str, devs))}")
+
+
 # ---------------------------------------------------------------------------
 class Index:
     """Owner of an ivfpq_index handle."""
@@ -157,6 +183,10 @@ def ivfpq_index_create(centroids, codebooks, nbits=8):
     _need(codebooks, torch.float32, "codebooks", 3)
     nlist, d = centroids.shape
     m = codebooks.shape[0]
+    if m < 1 or d % m or tuple(codebooks.shape[1:]) != (256, d // m):
+        raise ValueError(f"ivfpq_index_create: codebooks must be [m, 256, d/m] with d = {d}, "
+                         f"got {tuple(codebooks.shape)}")
+    _same_device("ivfpq_index_create", centroids, codebooks)
     h = C.c_void_p()
     _check("ivfpq_index_create",
            lib().ivfpq_index_create(d, nlist, m, nbits, _ptr(centroids), _ptr(codebooks),
@@ -185,6 +215,7 @@ def ivfpq_add(index, codes, list_ids, ids, stream=None):
     n = codes.shape[0]
     if codes.shape[1] != index.m or list_ids.shape[0] != n or ids.shape[0] != n:
         raise ValueError("ivfpq_add: inconsistent shapes")
+    _same_device("ivfpq_add", codes, list_ids, ids)
     _check("ivfpq_add", lib().ivfpq_add(index.handle, _ptr(codes), _ptr(list_ids), _ptr(ids), n,
                                          _stream(stream)))
 
@@ -195,12 +226,8 @@ def ivfpq_search(index, queries, nprobe, k, out_dist=None, out_ids=None, stream=
     nq = queries.shape[0]
     if queries.shape[1] != index.d:
         raise ValueError("ivfpq_search: query dimension mismatch")
-    if out_dist is None:
-        out_dist = torch.empty((nq, k), dtype=torch.float32, device=queries.device)
-    if out_ids is None:
-        out_ids = torch.empty((nq, k), dtype=torch.int64, device=queries.device)
-    _need(out_dist, torch.float32, "out_dist", 2)
-    _need(out_ids, torch.int64, "out_ids", 2)
+    out_dist = _out(out_dist, (nq, k), torch.float32, "out_dist", queries.device)
+    out_ids = _out(out_ids, (nq, k), torch.int64, "out_ids", queries.device)
     _check("ivfpq_search", lib().ivfpq_search(index.handle, _ptr(queries), nq, nprobe, k,
                                                _ptr(out_dist), _ptr(out_ids), _stream(stream)))
     return out_dist, out_ids
@@ -225,10 +252,12 @@ def ivfpq_search_preassigned(index, queries, probes, k, out_dist=None, out_ids=N
     _need(queries, torch.float32, "queries", 2)
     _need(probes, torch.int32, "probes", 2)
     nq, nprobe = probes.shape
-    if out_dist is None:
-        out_dist = torch.empty((nq, k), dtype=torch.float32, device=queries.device)
-    if out_ids is None:
-        out_ids = torch.empty((nq, k), dtype=torch.int64, device=queries.device)
+    if tuple(queries.shape) != (nq, index.d):
+        raise ValueError(f"ivfpq_search_preassigned: queries must be [{nq}, {index.d}] "
+                         f"(one row per probe row), got {tuple(queries.shape)}")
+    _same_device("ivfpq_search_preassigned", queries, probes)
+    out_dist = _out(out_dist, (nq, k), torch.float32, "out_dist", queries.device)
+    out_ids = _out(out_ids, (nq, k), torch.int64, "out_ids", queries.device)
     _check("ivfpq_search_preassigned",
            lib().ivfpq_search_preassigned(index.handle, _ptr(queries), nq, nprobe, _ptr(probes), k,
                                           _ptr(out_dist), _ptr(out_ids), _stream(stream)))
@@ -292,10 +321,9 @@ def flat_knn(db, queries, k, out_dist=None, out_ids=None, stream=None):
     nq = queries.shape[0]
     if queries.shape[1] != d:
         raise ValueError("flat_knn: dimension mismatch")
-    if out_dist is None:
-        out_dist = torch.empty((nq, k), dtype=torch.float32, device=queries.device)
-    if out_ids is None:
-        out_ids = torch.empty((nq, k), dtype=torch.int64, device=queries.device)
+    _same_device("flat_knn", db, queries)
+    out_dist = _out(out_dist, (nq, k), torch.float32, "out_dist", queries.device)
+    out_ids = _out(out_ids, (nq, k), torch.int64, "out_ids", queries.device)
     _check("flat_knn", lib().flat_knn(_ptr(db), n, d, _ptr(queries), nq, k, _ptr(out_dist),
                                        _ptr(out_ids), _stream(stream)))
     return out_dist, out_ids
@@ -311,6 +339,7 @@ def kmeans_lloyd(x, init, niter, stream=None):
     _need(init, torch.int64, "init", 1)
     n, d = x.shape
     k = init.shape[0]
+    _same_device("kmeans_lloyd", x, init)
     cent = torch.empty((k, d), dtype=torch.float32, device=x.device)
     assign = torch.empty((n,), dtype=torch.int32, device=x.device)
     obj = np.zeros(niter + 1, np.float64)
@@ -329,6 +358,9 @@ def pq_train(x, m, niter, init, stream=None):
     _need(x, torch.float32, "x", 2)
     _need(init, torch.int64, "init", 1)
     n, d = x.shape
+    if init.shape[0] != 256:
+        raise ValueError(f"pq_train: init must hold 256 seed rows, got {init.shape[0]}")
+    _same_device("pq_train", x, init)
     cb = torch.empty((m, 256, d // m), dtype=torch.float32, device=x.device)
     obj = np.zeros(niter + 1, np.float64)
     _check("pq_train", lib().pq_train(_ptr(x), n, d, m, niter, _ptr(init), _ptr(cb),
@@ -343,6 +375,10 @@ def ivfpq_knn_graph(index, x, self_ids, nprobe, k, stream=None):
     _need(x, torch.float32, "x", 2)
     _need(self_ids, torch.int64, "self_ids", 1)
     n = x.shape[0]
+    if x.shape[1] != index.d or self_ids.shape[0] != n:
+        raise ValueError(f"ivfpq_knn_graph: x must be [n, {index.d}] and self_ids [n], got "
+                         f"{tuple(x.shape)} and {tuple(self_ids.shape)}")
+    _same_device("ivfpq_knn_graph", x, self_ids)
     d = torch.empty((n, k), dtype=torch.float32, device=x.device)
     i = torch.empty((n, k), dtype=torch.int64, device=x.device)
     _check("ivfpq_knn_graph", lib().ivfpq_knn_graph(index.handle, _ptr(x), _ptr(self_ids), n,
@@ -356,6 +392,8 @@ def ivfpq_encode(index, x, stream=None):
     torch = _torch()
     _need(x, torch.float32, "x", 2)
     n = x.shape[0]
+    if x.shape[1] != index.d:
+        raise ValueError(f"ivfpq_encode: x must be [n, {index.d}], got {tuple(x.shape)}")
     lists = torch.empty((n,), dtype=torch.int32, device=x.device)
     codes = torch.empty((n, index.m), dtype=torch.uint8, device=x.device)
     _check("ivfpq_encode", lib().ivfpq_encode(index.handle, _ptr(x), n, _ptr(lists),
@@ -372,10 +410,9 @@ def knn_merge(dists, ids, k, out_dist=None, out_ids=None, stream=None):
     if tuple(ids.shape) != tuple(dists.shape):
         raise ValueError("knn_merge: dists and ids must have the same shape")
     S, nq, k_in = dists.shape
-    if out_dist is None:
-        out_dist = torch.empty((nq, k), dtype=torch.float32, device=dists.device)
-    if out_ids is None:
-        out_ids = torch.empty((nq, k), dtype=torch.int64, device=dists.device)
+    _same_device("knn_merge", dists, ids)
+    out_dist = _out(out_dist, (nq, k), torch.float32, "out_dist", dists.device)
+    out_ids = _out(out_ids, (nq, k), torch.int64, "out_ids", dists.device)
     _check("knn_merge", lib().knn_merge(_ptr(dists), _ptr(ids), nq, S, k_in, k, _ptr(out_dist),
                                          _ptr(out_ids), _stream(stream)))
     return out_dist, out_ids
@@ -385,10 +422,8 @@ def kselect(vals, k, out_vals=None, out_idx=None, stream=None):
     torch = _torch()
     _need(vals, torch.float32, "vals", 2)
     rows, cols = vals.shape
-    if out_vals is None:
-        out_vals = torch.empty((rows, k), dtype=torch.float32, device=vals.device)
-    if out_idx is None:
-        out_idx = torch.empty((rows, k), dtype=torch.int64, device=vals.device)
+    out_vals = _out(out_vals, (rows, k), torch.float32, "out_vals", vals.device)
+    out_idx = _out(out_idx, (rows, k), torch.int64, "out_idx", vals.device)
     _check("kselect", lib().kselect(_ptr(vals), rows, cols, k, _ptr(out_vals), _ptr(out_idx),
                                      _stream(stream)))
     return out_vals, out_idx
@@ -399,11 +434,11 @@ def kselect_noalloc(vals, k, out_vals, out_idx, stream=None):
     caller provides the outputs (fp32 and int64, [rows, k])."""
     torch = _torch()
     _need(vals, torch.float32, "vals", 2)
-    _need(out_vals, torch.float32, "out_vals", 2)
-    _need(out_idx, torch.int64, "out_idx", 2)
+    if out_vals is None or out_idx is None:
+        raise ValueError("kselect_noalloc: the caller provides out_vals and out_idx")
     rows, cols = vals.shape
-    if tuple(out_vals.shape) != (rows, k) or tuple(out_idx.shape) != (rows, k):
-        raise ValueError("kselect_noalloc: outputs must be [rows, k]")
+    out_vals = _out(out_vals, (rows, k), torch.float32, "out_vals", vals.device)
+    out_idx = _out(out_idx, (rows, k), torch.int64, "out_idx", vals.device)
     _check("kselect_noalloc", lib().kselect_noalloc(_ptr(vals), rows, cols, k, _ptr(out_vals),
                                                      _ptr(out_idx), _stream(stream)))
     return out_vals, out_idx
