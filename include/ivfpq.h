@@ -150,7 +150,8 @@ int ivfpq_search_probes(const ivfpq_index* index, const float* queries, int64_t 
  * ivfpq_search_preassigned -- lookup-table build, list scan and k-selection
  * for caller-given probes (the stages after the coarse quantizer).
  *  probes  device int32 [nq, nprobe], each in [0, nlist); a list given twice
- *          for one query contributes its vectors twice
+ *          for one query contributes its vectors twice; an id outside
+ *          [0, nlist) (for example -1 as padding) is skipped
  * Other arguments as ivfpq_search.
  */
 int ivfpq_search_preassigned(const ivfpq_index* index, const float* queries, int64_t nq,
