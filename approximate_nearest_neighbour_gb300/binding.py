@@ -220,12 +220,22 @@ def ivfpq_add(index, codes, list_ids, ids, stream=None):
                                          _stream(stream)))
 
 
+def _queries(fn, index, queries):
+    """Checks a [nq, d] fp32 query matrix against the index's d (the kernels
+    read d floats per row, so a narrower matrix would be read past its end)
+    before checking that it is a contiguous CUDA tensor."""
+    torch = _torch()
+    _need(queries, torch.float32, "queries", 2, device=False)
+    if queries.shape[1] != index.d:
+        raise ValueError(f"{fn}: query dimension {queries.shape[1]} does not match the "
+                         f"index's d = {index.d}")
+    _need(queries, torch.float32, "queries", 2)
+    return queries.shape[0]
+
+
 def ivfpq_search(index, queries, nprobe, k, out_dist=None, out_ids=None, stream=None):
     torch = _torch()
-    _need(queries, torch.float32, "queries", 2)
-    nq = queries.shape[0]
-    if queries.shape[1] != index.d:
-        raise ValueError("ivfpq_search: query dimension mismatch")
+    nq = _queries("ivfpq_search", index, queries)
     out_dist = _out(out_dist, (nq, k), torch.float32, "out_dist", queries.device)
     out_ids = _out(out_ids, (nq, k), torch.int64, "out_ids", queries.device)
     _check("ivfpq_search", lib().ivfpq_search(index.handle, _ptr(queries), nq, nprobe, k,
@@ -235,8 +245,7 @@ def ivfpq_search(index, queries, nprobe, k, out_dist=None, out_ids=None, stream=
 
 def ivfpq_search_probes(index, queries, nprobe, with_dist=True, stream=None):
     torch = _torch()
-    _need(queries, torch.float32, "queries", 2)
-    nq = queries.shape[0]
+    nq = _queries("ivfpq_search_probes", index, queries)
     probes = torch.empty((nq, nprobe), dtype=torch.int32, device=queries.device)
     coarse = (torch.empty((nq, nprobe), dtype=torch.float32, device=queries.device)
               if with_dist else None)

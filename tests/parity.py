@@ -1,7 +1,11 @@
 """Comparison rules between the CUDA path and the CPU oracle.
 
-Tolerance (from the floating-point analysis in the design doc): a GPU distance g
-matches an oracle distance D when |g - D| <= max(1e-4 |D|, 1e-5). Result ids
+Tolerance: a GPU distance g matches an oracle distance D when
+|g - D| <= max(1e-4 |D|, 1e-5). The GPU sums at most 64 fp32 table entries
+(ADC) or 128 fp32 squares (coarse and flat distances, direct form), each
+with a relative rounding error of 2^-24, so its relative error stays near
+1e-5; 1e-4 leaves a tenfold margin, and the absolute floor covers
+distances that cancel to nearly zero. Result ids
 are compared as sets after removing the boundary ties: every id whose oracle
 distance is below the k-th oracle distance by more than the tolerance must be
 returned, and every returned id must be a genuine candidate whose oracle

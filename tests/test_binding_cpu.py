@@ -58,3 +58,17 @@ def test_inputs_must_be_device_tensors(B):
         B.kselect(torch.zeros((4, 8)), 2)
     with pytest.raises(TypeError):
         B.kselect(torch.zeros((4, 8), dtype=torch.float64), 2)
+
+
+@pytest.mark.parametrize("fn", ["ivfpq_search_probes", "ivfpq_search"])
+def test_query_width_must_match_the_index(B, fn):
+    """The coarse kernel reads d floats per query row: a narrower (or wider)
+    query matrix is refused on the host, before anything else is checked."""
+    import torch
+    ix = B.Index(None, 8, 4, 2)  # a handle is never reached
+    q = torch.zeros((3, 5))
+    with pytest.raises(ValueError, match="dimension 5 does not match"):
+        if fn == "ivfpq_search":
+            B.ivfpq_search(ix, q, 2, 1)
+        else:
+            B.ivfpq_search_probes(ix, q, 2)

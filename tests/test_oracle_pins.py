@@ -124,6 +124,32 @@ def test_quantized_lut_fp8_scale_and_rounding():
     assert np.all(np.abs(Q - T)[normal] <= 2 ** -4 * T[normal])
 
 
+@pytest.mark.parametrize("top", [3.7, 0.01 * 448, 37 * 448, 2.0 ** -3])
+def test_quantized_lut_fp8_applies_one_scale_per_table_set(top):
+    """Tables whose largest entry is not 448: s = max T / 448, every entry is
+    stored as E4M3(T / s) and read back times s (one fp32 scale per table
+    set). The expected values go through torch's float8_e4m3fn cast of T / s,
+    so an oracle that stored T * s, or did not multiply back, fails."""
+    g = _rng(int(top * 1000) % 997)
+    T = g.uniform(0, 1, (32, 256)) * top
+    T[5, 200] = top  # the maximum
+    T[0, 0] = 0.0
+    s = top / 448.0
+    ref = torch.from_numpy(T / s).to(torch.float8_e4m3fn).to(torch.float64).numpy() * s
+    Q = oracle.quantize_lut(T, oracle.LUT_FP8)
+    assert np.array_equal(Q, ref)
+    assert Q[5, 200] == top and Q[0, 0] == 0.0
+    # relative rounding of E4M3 normals is at most 2^-4
+    normal = T / s >= 2 ** -6
+    assert np.all(np.abs(Q - T)[normal] <= 2 ** -4 * T[normal])
+    assert not np.array_equal(Q, T)
+
+
+def test_quantized_lut_fp8_all_zero_table_is_unchanged():
+    T = np.zeros((8, 256))
+    assert np.array_equal(oracle.quantize_lut(T, oracle.LUT_FP8), T)
+
+
 # --------------------------------------------------------------------------
 # IVF-PQ end to end on exactly representable data
 def _dyadic_index(seed, nlist, d, m, n, nq):
