@@ -53,6 +53,9 @@ SIGNATURES = {
     "kmeans_lloyd": (_I, [_VP, _I64, _I, _I, _I, _VP, _VP, _VP, _VP, _VP]),
     "pq_train": (_I, [_VP, _I64, _I, _I, _I, _VP, _VP, _VP, _VP]),
     "ivfpq_encode": (_I, [_VP, _VP, _I64, _VP, _VP, _VP]),
+    "ivfpq_residuals": (_I, [_VP, _I, _I, _VP, _I64, _VP, _VP, _VP]),
+    "ivfpq_encode_hinted": (_I, [_VP, _VP, _I64, _VP, _VP, _VP, C.POINTER(_I64), _VP]),
+    "ivfpq_repaired_queries": (_I, [_VP, C.POINTER(_I64), _VP]),
     "ivfpq_knn_graph": (_I, [_VP, _VP, _VP, _I64, _I, _I, _VP, _VP, _VP]),
     "ivfpq_device_check": (_I, [_VP]),
     "ivfpq_selftest_wait_timeout": (_I, [_I, _VP]),
@@ -408,6 +411,52 @@ def ivfpq_encode(index, x, stream=None):
     _check("ivfpq_encode", lib().ivfpq_encode(index.handle, _ptr(x), n, _ptr(lists),
                                                _ptr(codes), _stream(stream)))
     return lists, codes
+
+
+def ivfpq_residuals(centroids, x, stream=None):
+    """(nearest centroid int32 [n], residual x - centroid fp32 [n, d]) of device
+    fp32 x [n, d] against device fp32 centroids [nlist, d]."""
+    torch = _torch()
+    _need(centroids, torch.float32, "centroids", 2)
+    _need(x, torch.float32, "x", 2)
+    nlist, d = centroids.shape
+    n = x.shape[0]
+    if x.shape[1] != d:
+        raise ValueError(f"ivfpq_residuals: x must be [n, {d}], got {tuple(x.shape)}")
+    _same_device("ivfpq_residuals", centroids, x)
+    lists = torch.empty((n,), dtype=torch.int32, device=x.device)
+    resid = torch.empty((n, d), dtype=torch.float32, device=x.device)
+    _check("ivfpq_residuals", lib().ivfpq_residuals(_ptr(centroids), nlist, d, _ptr(x), n,
+                                                     _ptr(lists), _ptr(resid), _stream(stream)))
+    return lists, resid
+
+
+def ivfpq_encode_hinted(index, x, hint, list_ids=None, codes=None, stream=None):
+    """ivfpq_encode with a candidate list per row (int32 [n]): (list ids,
+    codes, rows that needed the full nearest-centroid search)."""
+    torch = _torch()
+    _need(x, torch.float32, "x", 2)
+    _need(hint, torch.int32, "hint", 1)
+    n = x.shape[0]
+    if x.shape[1] != index.d or hint.shape[0] != n:
+        raise ValueError(f"ivfpq_encode_hinted: x must be [n, {index.d}] and hint [n], got "
+                         f"{tuple(x.shape)} and {tuple(hint.shape)}")
+    _same_device("ivfpq_encode_hinted", x, hint)
+    list_ids = _out(list_ids, (n,), torch.int32, "list_ids", x.device)
+    codes = _out(codes, (n, index.m), torch.uint8, "codes", x.device)
+    searched = C.c_int64(0)
+    _check("ivfpq_encode_hinted",
+           lib().ivfpq_encode_hinted(index.handle, _ptr(x), n, _ptr(hint), _ptr(list_ids),
+                                     _ptr(codes), C.byref(searched), _stream(stream)))
+    return list_ids, codes, int(searched.value)
+
+
+def ivfpq_repaired_queries(index, stream=None):
+    """Queries re-scanned with full-length queues since the previous call."""
+    n = C.c_int64(0)
+    _check("ivfpq_repaired_queries",
+           lib().ivfpq_repaired_queries(index.handle, C.byref(n), _stream(stream)))
+    return int(n.value)
 
 
 def knn_merge(dists, ids, k, out_dist=None, out_ids=None, stream=None):

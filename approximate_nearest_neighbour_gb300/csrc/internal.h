@@ -6,6 +6,7 @@
 #include <stdint.h>
 
 #include <atomic>
+#include <mutex>
 #include <vector>
 
 #include "common.cuh"
@@ -148,6 +149,14 @@ struct ivfpq_index {
   int64_t* ids = nullptr;             // [nblocks * 32], -1 on padding slots
   std::vector<int64_t> h_list_len;    // host mirror of list_len
   int64_t max_list_len = 0;
+  // queries re-scanned with full-length queues since the last read
+  // (ivfpq_repaired_queries); device int64
+  unsigned long long* repaired = nullptr;
+  // per centroid, a lower bound (with rounding margins) of the squared
+  // distance to its nearest other centroid; computed on the first hinted
+  // encode (ivfpq_encode_hinted) under sep_mutex
+  float* cent_sep = nullptr;
+  std::mutex sep_mutex;
   // optional per-stage timing: one set of 5 events per profiled search
   struct EventSet {
     cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};

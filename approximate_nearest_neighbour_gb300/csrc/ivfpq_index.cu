@@ -237,6 +237,8 @@ extern "C" int ivfpq_index_create(int d, int nlist, int m, int nbits, const floa
   CREATE_CUDA(cudaMalloc(&cb_tmp, cb_n * sizeof(float)));
   CREATE_CUDA(cudaMalloc(&ix->list_len, size_t(nlist) * sizeof(int32_t)));
   CREATE_CUDA(cudaMalloc(&ix->list_block_off, size_t(nlist + 1) * sizeof(int64_t)));
+  CREATE_CUDA(cudaMalloc(&ix->repaired, sizeof(unsigned long long)));
+  CREATE_CUDA(cudaMemsetAsync(ix->repaired, 0, sizeof(unsigned long long), 0));
   CREATE_CUDA(cudaMemcpyAsync(ix->centroids, centroids, size_t(nlist) * d * sizeof(float),
                               cudaMemcpyDefault, 0));
   CREATE_CUDA(cudaMemcpyAsync(cb_tmp, codebooks, cb_n * sizeof(float), cudaMemcpyDefault, 0));
@@ -284,6 +286,8 @@ extern "C" int ivfpq_index_destroy(ivfpq_index* ix) {
   cudaFree(ix->list_block_off);
   cudaFree(ix->codes);
   cudaFree(ix->ids);
+  cudaFree(ix->repaired);
+  cudaFree(ix->cent_sep);
   for (auto& set : ix->ev_sets)
     for (auto& e : set.ev)
       if (e) cudaEventDestroy(e);

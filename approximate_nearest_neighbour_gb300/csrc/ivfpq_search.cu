@@ -116,18 +116,23 @@ int launch_scan_general(const ScanParams& p, int64_t nq, cudaStream_t s) {
 // Queries whose result may have lost an entry to a short warp queue: some
 // full queue (last key real) whose last key is not above the merged k-th
 // key. kth: merged distances [nq, k] (row's k-th at kth[q * k + k - 1]).
+// The number of flagged queries is added to *repaired.
 __global__ void warp_queue_check_kernel(const uint32_t* __restrict__ pkeys, int64_t nq,
                                         int groups, int kw, const float* __restrict__ kth,
-                                        int k, int* __restrict__ flags) {
+                                        int k, int* __restrict__ flags,
+                                        unsigned long long* __restrict__ repaired) {
   const int64_t q = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (q >= nq) return;
-  const uint32_t theta = __float_as_uint(kth[q * k + k - 1]);
   int f = 0;
-  for (int g = 0; g < groups; ++g) {
-    const uint32_t last = pkeys[(q * groups + g) * kw + kw - 1];
-    f |= last != kSentinelKey && last <= theta;
+  if (q < nq) {
+    const uint32_t theta = __float_as_uint(kth[q * k + k - 1]);
+    for (int g = 0; g < groups; ++g) {
+      const uint32_t last = pkeys[(q * groups + g) * kw + kw - 1];
+      f |= last != kSentinelKey && last <= theta;
+    }
+    flags[q] = f;
   }
-  flags[q] = f;
+  const unsigned c = __popc(__ballot_sync(kFullMask, f));
+  if ((threadIdx.x & 31) == 0 && c) atomicAdd(repaired, (unsigned long long)c);
 }
 
 const size_t kMaxEventSets = 4096;
@@ -241,8 +246,8 @@ int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int npro
     // repair the queries whose merged result a short queue may have cut
     int* flags = nullptr;
     IVFPQ_TRY(ws.alloc(&flags, size_t(nq)));
-    warp_queue_check_kernel<<<unsigned(ceil_div(nq, 256)), 256, 0, s>>>(p.pkeys, nq, groups, kw,
-                                                                       out_dist, k, flags);
+    warp_queue_check_kernel<<<unsigned(ceil_div(nq, 256)), 256, 0, s>>>(
+        p.pkeys, nq, groups, kw, out_dist, k, flags, ix->repaired);
     IVFPQ_LAUNCHED();
     ScanParams r = p;
     r.qmask = flags;
@@ -390,6 +395,18 @@ extern "C" int ivfpq_set_profiling(ivfpq_index* ix, int enable) {
   ix->profile = enable != 0;
   ix->ev_used = 0;
   ix->cur_set = -1;
+  return IVFPQ_OK;
+}
+
+extern "C" int ivfpq_repaired_queries(const ivfpq_index* ix, int64_t* count, void* stream) {
+  clear_error();
+  IVFPQ_REQUIRE(ix && count, "ivfpq_repaired_queries: null pointer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned long long h = 0;
+  IVFPQ_CUDA(cudaMemcpyAsync(&h, ix->repaired, sizeof(h), cudaMemcpyDeviceToHost, s));
+  IVFPQ_CUDA(cudaMemsetAsync(ix->repaired, 0, sizeof(h), s));
+  IVFPQ_CUDA(cudaStreamSynchronize(s));
+  *count = int64_t(h);
   return IVFPQ_OK;
 }
 

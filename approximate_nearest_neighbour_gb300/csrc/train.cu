@@ -126,6 +126,98 @@ __global__ void encode_kernel(const float* __restrict__ x, int64_t n, int d, int
   }
 }
 
+// r[i] = x[i] - c[lists[i]] (rows of d floats)
+__global__ void residual_kernel(const float* __restrict__ x, int64_t n, int d,
+                                const float* __restrict__ cent, const int32_t* __restrict__ lists,
+                                float* __restrict__ r) {
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n * d;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t row = i / d;
+    r[i] = x[i] - cent[int64_t(lists[row]) * d + int(i - row * d)];
+  }
+}
+
+// Lower bound of each centroid's squared distance to its nearest other
+// centroid, from the two nearest centroids of every centroid (k = 2 search of
+// the centroids among themselves; one of the two is the centroid itself).
+// The search selects on tensor-core distances whose error is below
+// 2^-22 (|c|^2 + |c'|^2) and returns the direct-form fp32 distance of what it
+// selected, so the true separation is at least the returned one minus
+// 2^-21 (|c|^2 + max |c'|^2) and a relative rounding term; the bound
+// subtracts eight times that (2^-18) and 1e-4 relative.
+__global__ void separation_kernel(const float* __restrict__ d2, const int64_t* __restrict__ i2,
+                                  int nlist, const float* __restrict__ norms,
+                                  const float* __restrict__ max_norm, float* __restrict__ sep) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= nlist) return;
+  const float s2 = i2[2 * int64_t(c)] == c ? d2[2 * int64_t(c) + 1] : d2[2 * int64_t(c)];
+  const float margin = 0x1p-18f * (norms[c] + *max_norm);
+  sep[c] = fmaxf(0.f, s2 * (1.f - 1e-4f) - margin);
+}
+
+// Hint check, one warp per row: the hint h is x's nearest centroid, and the
+// only one, if 4 ||x - c_h||^2 < sep[h] (the triangle inequality: for any
+// other centroid c, ||x - c|| >= ||c_h - c|| - ||x - c_h|| > ||x - c_h||;
+// Elkan, "Using the triangle inequality to accelerate k-means", ICML 2003,
+// Lemma 1). Writes the hint as the list of a row that passes and flags the
+// others (need[r] = 1) for a full search.
+__global__ void hint_check_kernel(const float* __restrict__ x, int64_t n, int d,
+                                  const float* __restrict__ cent, int nlist,
+                                  const float* __restrict__ sep, const int32_t* __restrict__ hint,
+                                  int32_t* __restrict__ lists, int* __restrict__ need) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = int64_t(gridDim.x) * (blockDim.x >> 5);
+  for (int64_t r = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); r < n;
+       r += warps) {
+    const int h = hint[r];
+    bool pass = false;
+    if (h >= 0 && h < nlist) {
+      const float* xr = x + r * d;
+      const float* cr = cent + int64_t(h) * d;
+      float a = 0.f;
+      for (int t = lane; t < d; t += 32) {
+        const float df = xr[t] - cr[t];
+        a = fmaf(df, df, a);
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o /= 2) a += __shfl_xor_sync(kFullMask, a, o);
+      pass = 4.f * a * (1.f + 1e-4f) < sep[h];
+    }
+    if (lane == 0) {
+      lists[r] = pass ? h : -1;
+      need[r] = pass ? 0 : 1;
+    }
+  }
+}
+
+// rows[pos[i]] = i for the flagged rows (pos = exclusive prefix sum of need)
+__global__ void compact_kernel(const int* __restrict__ need, const int* __restrict__ pos,
+                               int64_t n, int32_t* __restrict__ rows) {
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x)
+    if (need[i]) rows[pos[i]] = int32_t(i);
+}
+
+// y[i] = x[rows[i]] (rows of d floats)
+__global__ void gather_rows_kernel(const float* __restrict__ x, int d,
+                                   const int32_t* __restrict__ rows, int64_t cnt,
+                                   float* __restrict__ y) {
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < cnt * d;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t r = i / d;
+    y[i] = x[int64_t(rows[r]) * d + int(i - r * d)];
+  }
+}
+
+// lists[rows[i]] = found[i]
+__global__ void scatter_lists_kernel(const int32_t* __restrict__ rows,
+                                     const int32_t* __restrict__ found, int64_t cnt,
+                                     int32_t* __restrict__ lists) {
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < cnt;
+       i += int64_t(gridDim.x) * blockDim.x)
+    lists[rows[i]] = found[i];
+}
+
 }  // namespace
 
 namespace {
@@ -279,5 +371,138 @@ extern "C" int ivfpq_encode(const ivfpq_index* ix, const float* x, int64_t n, in
                                                       ix->centroids, list_ids, ix->codebooks,
                                                       codes);
   IVFPQ_LAUNCHED();
+  return IVFPQ_OK;
+}
+
+namespace ivfpq {
+namespace {
+
+// The separation bounds of the index's centroids (computed once).
+int centroid_separation(const ivfpq_index* cix, cudaStream_t s) {
+  auto* ix = const_cast<ivfpq_index*>(cix);
+  std::lock_guard<std::mutex> lock(ix->sep_mutex);
+  if (ix->cent_sep) return IVFPQ_OK;
+  const int nlist = ix->nlist;
+  float* sep = nullptr;
+  IVFPQ_CUDA(cudaMalloc(&sep, size_t(nlist) * sizeof(float)));
+  struct Guard {
+    float*& p;
+    ~Guard() {
+      if (p) cudaFree(p);
+    }
+  } guard{sep};
+  if (nlist == 1) {
+    const float inf = INFINITY;
+    IVFPQ_CUDA(cudaMemcpyAsync(sep, &inf, sizeof(float), cudaMemcpyHostToDevice, s));
+  } else {
+    Workspace ws(s);
+    float* d2 = nullptr;
+    int64_t* i2 = nullptr;
+    float* mx = nullptr;
+    IVFPQ_TRY(ws.alloc(&d2, size_t(nlist) * 2));
+    IVFPQ_TRY(ws.alloc(&i2, size_t(nlist) * 2));
+    IVFPQ_TRY(ws.alloc(&mx, 1));
+    SelectOut o;
+    o.kind = OutKind::Float;
+    o.vals = d2;
+    o.idx64 = i2;
+    TcOperand xo;
+    xo.hi = ix->cent_hi;
+    xo.lo = ix->cent_lo;
+    xo.norms = ix->cent_norms;
+    IVFPQ_TRY(knn_by_tiles(ix->centroids, nlist, ix->centroids, nlist, ix->d, 2, o, s,
+                           ix->cent_hi ? &xo : nullptr));
+    size_t red_bytes = 0;
+    IVFPQ_CUDA(cub::DeviceReduce::Max(nullptr, red_bytes, ix->cent_norms, mx, nlist, s));
+    uint8_t* red_tmp = nullptr;
+    IVFPQ_TRY(ws.alloc(&red_tmp, red_bytes));
+    IVFPQ_CUDA(cub::DeviceReduce::Max(red_tmp, red_bytes, ix->cent_norms, mx, nlist, s));
+    separation_kernel<<<unsigned(ceil_div(nlist, 256)), 256, 0, s>>>(d2, i2, nlist,
+                                                                     ix->cent_norms, mx, sep);
+    IVFPQ_LAUNCHED();
+  }
+  IVFPQ_CUDA(cudaStreamSynchronize(s));
+  ix->cent_sep = sep;
+  sep = nullptr;
+  return IVFPQ_OK;
+}
+
+}  // namespace
+}  // namespace ivfpq
+
+extern "C" int ivfpq_residuals(const float* centroids, int nlist, int d, const float* x, int64_t n,
+                               int32_t* list_ids, float* residuals, void* stream) {
+  clear_error();
+  IVFPQ_REQUIRE(d >= 1 && nlist >= 1, "ivfpq_residuals: bad sizes (d=%d nlist=%d)", d, nlist);
+  IVFPQ_REQUIRE(n >= 0 && n < (int64_t(1) << 31), "ivfpq_residuals: n=%lld", (long long)n);
+  if (n == 0) return IVFPQ_OK;
+  IVFPQ_REQUIRE(centroids && x && list_ids && residuals, "ivfpq_residuals: null pointer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  SelectOut o;
+  o.kind = OutKind::Probes;
+  o.idx32 = list_ids;
+  IVFPQ_TRY(knn_by_tiles(x, n, centroids, nlist, d, 1, o, s));
+  residual_kernel<<<grid1(n * d, 256), 256, 0, s>>>(x, n, d, centroids, list_ids, residuals);
+  IVFPQ_LAUNCHED();
+  return IVFPQ_OK;
+}
+
+extern "C" int ivfpq_encode_hinted(const ivfpq_index* ix, const float* x, int64_t n,
+                                   const int32_t* hint, int32_t* list_ids, uint8_t* codes,
+                                   int64_t* n_searched, void* stream) {
+  clear_error();
+  IVFPQ_REQUIRE(ix, "ivfpq_encode_hinted: null index");
+  IVFPQ_REQUIRE(n >= 0 && n < (int64_t(1) << 31), "ivfpq_encode_hinted: n=%lld", (long long)n);
+  IVFPQ_REQUIRE(ix->dsub <= 32, "ivfpq_encode_hinted: d/m=%d above 32", ix->dsub);
+  if (n_searched) *n_searched = 0;
+  if (n == 0) return IVFPQ_OK;
+  IVFPQ_REQUIRE(x && hint && list_ids && codes, "ivfpq_encode_hinted: null pointer");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  IVFPQ_TRY(centroid_separation(ix, s));
+  Workspace ws(s);
+  int *need = nullptr, *pos = nullptr;
+  IVFPQ_TRY(ws.alloc(&need, size_t(n)));
+  IVFPQ_TRY(ws.alloc(&pos, size_t(n)));
+  hint_check_kernel<<<grid1(n * 32, 256), 256, 0, s>>>(x, n, ix->d, ix->centroids, ix->nlist,
+                                                        ix->cent_sep, hint, list_ids, need);
+  IVFPQ_LAUNCHED();
+  size_t scan_bytes = 0;
+  IVFPQ_CUDA(cub::DeviceScan::ExclusiveSum(nullptr, scan_bytes, need, pos, n, s));
+  uint8_t* scan_tmp = nullptr;
+  IVFPQ_TRY(ws.alloc(&scan_tmp, scan_bytes));
+  IVFPQ_CUDA(cub::DeviceScan::ExclusiveSum(scan_tmp, scan_bytes, need, pos, n, s));
+  int tail[2] = {0, 0};
+  IVFPQ_CUDA(cudaMemcpyAsync(&tail[0], pos + n - 1, sizeof(int), cudaMemcpyDeviceToHost, s));
+  IVFPQ_CUDA(cudaMemcpyAsync(&tail[1], need + n - 1, sizeof(int), cudaMemcpyDeviceToHost, s));
+  IVFPQ_CUDA(cudaStreamSynchronize(s));
+  const int64_t cnt = int64_t(tail[0]) + tail[1];
+  if (cnt > 0) {
+    // the rows whose hint could not be confirmed: a full nearest-centroid search
+    int32_t *rows = nullptr, *found = nullptr;
+    float* y = nullptr;
+    IVFPQ_TRY(ws.alloc(&rows, size_t(cnt)));
+    IVFPQ_TRY(ws.alloc(&found, size_t(cnt)));
+    IVFPQ_TRY(ws.alloc(&y, size_t(cnt) * ix->d));
+    compact_kernel<<<grid1(n, 256), 256, 0, s>>>(need, pos, n, rows);
+    IVFPQ_LAUNCHED();
+    gather_rows_kernel<<<grid1(cnt * ix->d, 256), 256, 0, s>>>(x, ix->d, rows, cnt, y);
+    IVFPQ_LAUNCHED();
+    SelectOut o;
+    o.kind = OutKind::Probes;
+    o.idx32 = found;
+    TcOperand xo;
+    xo.hi = ix->cent_hi;
+    xo.lo = ix->cent_lo;
+    xo.norms = ix->cent_norms;
+    IVFPQ_TRY(knn_by_tiles(y, cnt, ix->centroids, ix->nlist, ix->d, 1, o, s,
+                           ix->cent_hi ? &xo : nullptr));
+    scatter_lists_kernel<<<grid1(cnt, 256), 256, 0, s>>>(rows, found, cnt, list_ids);
+    IVFPQ_LAUNCHED();
+  }
+  encode_kernel<<<grid1(n * ix->m, 256), 256, 0, s>>>(x, n, ix->d, ix->m, ix->dsub, ix->dsub4,
+                                                      ix->centroids, list_ids, ix->codebooks,
+                                                      codes);
+  IVFPQ_LAUNCHED();
+  if (n_searched) *n_searched = cnt;
   return IVFPQ_OK;
 }

@@ -3,7 +3,8 @@
 This module only draws random numbers and arranges them; it holds none of the
 search method's arithmetic (no distances, no quantization, no selection). Both
 the tests (which feed the same arrays to the CPU oracle and to the CUDA path)
-and the benchmark use it. It depends on numpy alone.
+and the benchmark use it. It depends on numpy; the device-side draws of large
+databases use torch's CUDA generator.
 
 Recipe (stand-in for the pages' Sift1M / Sift1B / Deep1B / Yfcc100M datasets,
 which are not available here):
@@ -12,11 +13,15 @@ which are not available here):
   centre_c + sigma * N(0, I). Component weights are uniform, or Zipf with
   exponent 0.5 (p_c proportional to (c + 1)^-0.5 in component order).
 * Coarse centroids are the true mixture centres (nlist = number of components).
-* Large IVF-PQ workloads are generated directly in compressed form: list sizes
-  are a multinomial draw over the component weights, every code byte is uniform
-  over the 256 reproduction values, and the PQ codebooks are samples of the
-  residual distribution (codeword = sigma * N(0, I_dsub)). A stored vector is
-  therefore exactly centroid + decoded residual.
+* Large databases as raw vectors, drawn on the device in seeded blocks so
+  that any row range can be drawn again: the component of every row
+  (`device_labels`), then the rows (`device_points`). The index is built from
+  them by the library's own index preparation (indexing.py).
+* Large databases in compressed form (`compressed_index`): list sizes from a
+  multinomial draw over the component weights, every code byte uniform over
+  the 256 reproduction values, and PQ codebooks sampled from the residual
+  distribution (codeword = sigma * N(0, I_dsub)); a stored vector is exactly
+  centroid + decoded residual.
 * Queries are drawn from the same mixture.
 
 Seeds: 20170228 + 1000 * workload number; sub-streams 0 = centres,
@@ -191,6 +196,80 @@ def tiny_raw(w: IVFPQWorkload = IVFPQ_TINY, n: int | None = None):
     x = mixture_points(g, cent, comps, w.sigma)
     init = rng(w.number, STREAM_TRAIN).choice(n, size=256, replace=False).astype(np.int64)
     return cent, x, init
+
+
+# ---------------------------------------------------------------------------
+# large databases as raw vectors drawn on the device
+
+NOISE_BLOCK = 1 << 22   # rows per seeded block of device-side noise
+LABEL_BLOCK = 1 << 24   # rows per seeded block of device-side labels
+TRAIN_ROWS = 262_144    # rows of the product-quantizer training sample
+
+
+def _block_seed(number: int, role: int, block: int, salt: int) -> int:
+    ss = np.random.SeedSequence([BASE_SEED + 1000 * number, STREAM_DB, role + salt, block])
+    return int(ss.generate_state(1, np.uint64)[0] >> np.uint64(1))
+
+
+def device_labels(number: int, n: int, weights: np.ndarray, device, salt: int = 0):
+    """Mixture component of each of n database rows (torch int32 [n] on
+    `device`), drawn in blocks of LABEL_BLOCK rows from generators seeded by
+    (workload, block): uniform integers for uniform weights, else inverse-CDF
+    sampling of the weights."""
+    import torch
+    out = torch.empty((n,), dtype=torch.int32, device=device)
+    ncomp = weights.shape[0]
+    uniform = bool(np.all(weights == weights[0]))
+    cdf = np.cumsum(weights)
+    cdf[-1] = 1.0
+    cdf_d = torch.from_numpy(cdf).to(device)
+    for blk, a in enumerate(range(0, n, LABEL_BLOCK)):
+        b = min(n, a + LABEL_BLOCK)
+        g = torch.Generator(device=device)
+        g.manual_seed(_block_seed(number, 100, blk, salt))
+        if uniform:
+            out[a:b] = torch.randint(0, ncomp, (b - a,), generator=g, device=device,
+                                     dtype=torch.int32)
+        else:
+            u = torch.rand((b - a,), generator=g, device=device, dtype=torch.float64)
+            out[a:b] = torch.searchsorted(cdf_d, u, right=True).clamp_(max=ncomp - 1).int()
+    return out
+
+
+def device_points(number: int, cent, labels_dev, sigma: float, start: int, count: int,
+                  salt: int = 0):
+    """Rows [start, start + count) of a mixture database, drawn on cent's
+    device (torch fp32 [count, d]): the centre of each row's component plus
+    sigma * N(0, I). Row i's noise is row i mod NOISE_BLOCK of block
+    i // NOISE_BLOCK, which comes from a generator seeded by (workload,
+    block), so the same rows come back whatever range they are drawn in."""
+    import torch
+    d = cent.shape[1]
+    dev = cent.device
+    out = torch.empty((count, d), dtype=torch.float32, device=dev)
+    if count == 0:
+        return out
+    for blk in range(start // NOISE_BLOCK, (start + count - 1) // NOISE_BLOCK + 1):
+        g = torch.Generator(device=dev)
+        g.manual_seed(_block_seed(number, 200, blk, salt))
+        z = torch.randn((NOISE_BLOCK, d), generator=g, device=dev, dtype=torch.float32)
+        lo = max(start, blk * NOISE_BLOCK)
+        hi = min(start + count, (blk + 1) * NOISE_BLOCK)
+        out[lo - start:hi - start] = z[lo - blk * NOISE_BLOCK:hi - blk * NOISE_BLOCK]
+        del z
+    out.mul_(sigma)
+    out.add_(cent[labels_dev[start:start + count].long()])
+    return out
+
+
+def training_rows(number: int, n: int) -> tuple:
+    """(rows used to train the product quantizer, 256 of them that seed its
+    codewords). The database rows are in random order, so its first
+    min(n, TRAIN_ROWS) rows are a seeded random sample of it; the seeds are
+    256 distinct rows of that sample."""
+    ntrain = min(n, TRAIN_ROWS)
+    init = rng(number, STREAM_TRAIN).choice(ntrain, size=256, replace=False).astype(np.int64)
+    return ntrain, init
 
 
 def random_rows(rows: int, cols: int, seed: int, kind: str = "normal") -> np.ndarray:

@@ -324,6 +324,55 @@ int ivfpq_encode(const ivfpq_index* index, const float* x, int64_t n, int32_t* l
                  uint8_t* codes, void* stream);
 
 /*
+ * ivfpq_residuals -- nearest coarse centroid of each vector and the residual
+ * (vector minus that centroid), the training input of the product quantizer.
+ * Source: "Custom 8-bit floating point value format ...", index construction
+ * steps 1-2 (each vector belongs to the cluster of its nearest centroid; the
+ * residual is the vector minus the centroid); "Billion-scale similarity
+ * search with GPUs", section 5 (the product quantizer encodes residuals).
+ *  centroids  device fp32 [nlist, d];  x  device fp32 [n, d], n < 2^31
+ *  list_ids   device int32 [n] (out): nearest centroid (exact distances;
+ *             equal distances go to either centroid)
+ *  residuals  device fp32 [n, d] (out): x - centroids[list_ids]
+ * Asynchronous. Errors: INVALID_ARG, OOM, CUDA.
+ */
+int ivfpq_residuals(const float* centroids, int nlist, int d, const float* x, int64_t n,
+                    int32_t* list_ids, float* residuals, void* stream);
+
+/*
+ * ivfpq_encode_hinted -- ivfpq_encode for callers that know a likely list of
+ * each vector (the previous assignment of an iterative clustering, or the
+ * cluster a vector was drawn from). Same results as ivfpq_encode: the hint h
+ * of row r is accepted only when 4 ||x_r - c_h||^2 is below a lower bound of
+ * the squared distance from c_h to its nearest other centroid, which proves
+ * by the triangle inequality that c_h is the nearest centroid and the only
+ * one (Elkan, "Using the triangle inequality to accelerate k-means", ICML
+ * 2003, Lemma 1); every other row (a wrong, doubtful or out-of-range hint)
+ * gets the full nearest-centroid search of ivfpq_encode. The first call on an
+ * index computes the centroids' separations once (a k = 2 search of the
+ * centroids among themselves) and keeps them with the index.
+ *  hint        device int32 [n]: a list id per row (any value accepted)
+ *  n_searched  HOST int64 (out, may be NULL): rows that needed the full search
+ * Other arguments as ivfpq_encode. Synchronizes `stream` (the number of rows
+ * to search sizes that search). Errors: INVALID_ARG, OOM, CUDA.
+ */
+int ivfpq_encode_hinted(const ivfpq_index* index, const float* x, int64_t n, const int32_t* hint,
+                        int32_t* list_ids, uint8_t* codes, int64_t* n_searched, void* stream);
+
+/*
+ * ivfpq_repaired_queries -- the number of queries that searches of this
+ * index re-scanned since the previous call (or since creation), then resets
+ * it; a measurement aid. The register-codebook list scan keeps per warp a
+ * queue shorter than k; a query for which one warp may have held more of the
+ * k best than its queue is detected after the merge and scanned again with
+ * full-length queues, so results do not depend on it. Synchronizes `stream`;
+ * searches still running on other streams may not be counted yet.
+ *  count  HOST int64 (out)
+ * Errors: INVALID_ARG, CUDA.
+ */
+int ivfpq_repaired_queries(const ivfpq_index* index, int64_t* count, void* stream);
+
+/*
  * knn_merge -- final k-selection over the results of S index shards.
  * Source: sharding ("Billion-scale similarity search with GPUs", section 5,
  * multi-GPU): every shard holds part of the database and answers all queries;

@@ -80,6 +80,12 @@ def test_host_side_argument_errors_of_the_other_entries(lib):
         lambda: lib.pq_train(vp, 100, 16, 4, 1, vp, vp, vp, None),
         # encoder / graph / preassigned search without an index
         lambda: lib.ivfpq_encode(None, vp, 5, vp, vp, None),
+        lambda: lib.ivfpq_encode_hinted(None, vp, 5, vp, vp, vp, None, None),
+        lambda: lib.ivfpq_repaired_queries(None, None, None),
+        # residuals: bad d, no centroids, null outputs
+        lambda: lib.ivfpq_residuals(vp, 4, 0, vp, 5, vp, vp, None),
+        lambda: lib.ivfpq_residuals(vp, 0, 8, vp, 5, vp, vp, None),
+        lambda: lib.ivfpq_residuals(vp, 4, 8, vp, 5, None, vp, None),
         lambda: lib.ivfpq_knn_graph(None, vp, vp, 5, 1, 1, vp, vp, None),
         lambda: lib.ivfpq_search_preassigned(None, vp, 1, 1, vp, 1, vp, vp, None),
         lambda: lib.ivfpq_search_probes(None, vp, 1, 1, vp, vp, None),

@@ -43,7 +43,7 @@ def test_flat_full_size_sampled(B, k):
     import torch
     db, q = S.flat_database(S.FLAT_1M)
     gd, gi = _flat(B, db, q, k)
-    rows = np.random.default_rng(k).choice(q.shape[0], 6, replace=False)
+    rows = np.random.default_rng(k).choice(q.shape[0], 64, replace=False)
     od, oi = oracle.flat_knn(db, q[rows], k + 64)
     compare_knn(gd[rows], gi[rows], od, oi, context=f"flat full k={k}")
 

@@ -272,7 +272,9 @@ def test_bad_list_ids_leave_index_unchanged(B):
 # ---------------------------------------------------------------------------
 # full-size workloads, sampled queries (the launch configuration the
 # benchmark times: all queries in one call)
-def _full(B, w, nprobes, ks, nsample=6):
+def _full(B, w, nprobes, ks, nsample):
+    """The workload in compressed form (codes and codebooks drawn directly,
+    so every input of the oracle comes from the seeded generator)."""
     import torch
     data = S.compressed_index(w)
     q = S.queries(w.number, data.cent, data.weights, w.sigma, w.nq)
@@ -282,24 +284,122 @@ def _full(B, w, nprobes, ks, nsample=6):
     for nprobe in nprobes:
         for k in ks:
             search_and_check(B, ix, data.cent, data.cb, lists, q, nprobe, k, rows=rows,
-                             context=f"{w.name} nprobe={nprobe} k={k}")
+                             context=f"{w.name} compressed nprobe={nprobe} k={k}")
     del ix
     torch.cuda.empty_cache()
 
 
 @pytest.mark.slow
-def test_full_mid(B):
-    _full(B, S.IVFPQ_MID, (16, 64), (100,))
+def test_full_mid_compressed(B):
+    _full(B, S.IVFPQ_MID, (16, 64), (100,), 64)
 
 
 @pytest.mark.slow
-def test_full_large(B):
-    _full(B, S.IVFPQ_LARGE, (64,), (100,))
+def test_full_large_compressed(B):
+    _full(B, S.IVFPQ_LARGE, (64,), (100,), 256)
 
 
 @pytest.mark.slow
-def test_full_billion(B):
-    _full(B, S.IVFPQ_BILLION, (128,), (1, 100, 1000), nsample=4)
+def test_full_billion_compressed(B):
+    _full(B, S.IVFPQ_BILLION, (128,), (1, 100, 1000), 64)
+
+
+def _encoded(w):
+    import torch
+    from approximate_nearest_neighbour_gb300 import indexing
+    return indexing.workload_index(w, torch.device("cuda"))
+
+
+def _check_encoding(B, wi, w, nrows=512):
+    """The stored list and code of rows of the built index against the
+    oracle's nearest centroid (full sort) and nearest-codeword encoding of the
+    same rows, drawn again from the generator."""
+    import torch
+    rows = np.sort(np.random.default_rng(w.number + 1).choice(S.NOISE_BLOCK, nrows,
+                                                               replace=False))
+    x = S.device_points(w.number, wi.cent_dev, wi.labels, w.sigma, 0, S.NOISE_BLOCK)[
+        torch.as_tensor(rows, device="cuda")].cpu().numpy()
+    r_d = torch.as_tensor(rows, device="cuda")
+    lists = wi.lists[r_d].cpu().numpy()
+    codes = wi.codes[r_d].cpu().numpy()
+    ol, _ = oracle.coarse(x, wi.cent, 1)
+    assert np.array_equal(lists, ol[:, 0]), f"{w.name}: nearest centroid"
+    cb = wi.codebooks.cpu().numpy()
+    resid = x.astype(np.float64) - wi.cent[lists].astype(np.float64)
+    oc = oracle.pq_encode(resid.astype(np.float32), cb)
+    dsub = cb.shape[2]
+    for r, j in np.argwhere(oc != codes):
+        sub = resid[r, j * dsub:(j + 1) * dsub]
+        dg = ((sub - cb[j, codes[r, j]].astype(np.float64)) ** 2).sum()
+        do = ((sub - cb[j, oc[r, j]].astype(np.float64)) ** 2).sum()
+        assert dg - do <= 1e-5 * max(do, 1e-6), f"{w.name}: code of row {rows[r]}, j={j}"
+
+
+def _full_encoded(B, wi, w, nprobes, ks, nsample):
+    """The workload's index built from raw vectors by the library's training
+    and encoding (their own parity is checked in test_index_build_gpu.py and
+    by _check_encoding on this index); the search oracle reads the stored
+    codes of the probed lists as its input."""
+    import torch
+    from approximate_nearest_neighbour_gb300 import indexing
+    cb = wi.codebooks.cpu().numpy()
+    q = S.queries(w.number, wi.cent, wi.weights, w.sigma, w.nq)
+    rows = np.random.default_rng(w.number).choice(w.nq, nsample, replace=False)
+    gp, _ = B.ivfpq_search_probes(wi.index, _t(q[rows]), max(nprobes), with_dist=False)
+    torch.cuda.synchronize()
+    codes_h, lists_h, ids_h = indexing.lists_on_host(wi, np.unique(gp.cpu().numpy()))
+    lists = oracle.to_lists(codes_h, lists_h, ids_h, wi.cent.shape[0])
+    del codes_h, lists_h, ids_h
+    B.ivfpq_repaired_queries(wi.index)
+    for nprobe in nprobes:
+        for k in ks:
+            search_and_check(B, wi.index, wi.cent, cb, lists, q, nprobe, k, rows=rows,
+                             context=f"{w.name} encoded nprobe={nprobe} k={k}")
+            print(f"{w.name} nprobe={nprobe} k={k}: queries re-scanned with full queues "
+                  f"{B.ivfpq_repaired_queries(wi.index)} of {w.nq}")
+
+
+@pytest.mark.slow
+def test_full_mid_encoded(B):
+    import torch
+    w = S.IVFPQ_MID
+    wi = _encoded(w)
+    assert np.all(np.diff(wi.objective) <= 1e-6 * wi.objective[0])
+    _check_encoding(B, wi, w)
+    _full_encoded(B, wi, w, (16, 64), (100,), 64)
+    del wi
+    torch.cuda.empty_cache()
+
+
+@pytest.fixture(scope="module")
+def large_encoded(B):
+    import torch
+    wi = _encoded(S.IVFPQ_LARGE)
+    yield wi
+    del wi
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.slow
+def test_full_large_encoded(B, large_encoded):
+    w = S.IVFPQ_LARGE
+    wi = large_encoded
+    assert np.all(np.diff(wi.objective) <= 1e-6 * wi.objective[0])
+    print(f"{w.name}: rows searched in full by the encoder {wi.searched}")
+    _check_encoding(B, wi, w)
+    _full_encoded(B, wi, w, (64,), (100,), 256)
+
+
+@pytest.mark.slow
+def test_full_billion_encoded(B):
+    import torch
+    w = S.IVFPQ_BILLION
+    wi = _encoded(w)
+    print(f"{w.name}: rows searched in full by the encoder {wi.searched}")
+    _check_encoding(B, wi, w)
+    _full_encoded(B, wi, w, (128,), (1, 100, 1000), 64)
+    del wi
+    torch.cuda.empty_cache()
 
 
 # ---------------------------------------------------------------------------
@@ -334,22 +434,32 @@ def test_reduced_tables_follow_the_oracle_variant(B, lut, rtol, min_recall, m, d
 
 @pytest.mark.slow
 @pytest.mark.parametrize("lut,gate", [("fp16", 0.99), ("fp8", 0.95)])
-def test_full_large_reduced_table_recall_gates(B, lut, gate):
-    """Large workload (2e8 vectors, m = 32, nprobe = 64, k = 100): recall@100
-    of the fp16 / E4M3 table variants against the fp32 oracle on a seeded
-    sample of 256 queries (gates: 0.99 and 0.95)."""
+def test_full_large_reduced_table_recall_gates(B, large_encoded, lut, gate):
+    """Large workload (2e8 vectors, m = 32, nprobe = 64, k = 100; the index
+    built from raw vectors with trained codebooks): recall@100 of the fp16 /
+    E4M3 table variants against the fp32 oracle on a seeded sample of 256
+    queries (gates: 0.99 and 0.95)."""
     import torch
+    from approximate_nearest_neighbour_gb300 import indexing
     w = S.IVFPQ_LARGE
-    data = S.compressed_index(w)
-    q = S.queries(w.number, data.cent, data.weights, w.sigma, w.nq)
-    gp, gd, gi = _variant_run(B, data, q, 64, 100, lut)
+    wi = large_encoded
+    q = S.queries(w.number, wi.cent, wi.weights, w.sigma, w.nq)
+    B.ivfpq_set_lut_type(wi.index, lut)
+    try:
+        gp, _ = B.ivfpq_search_probes(wi.index, _t(q), 64, with_dist=False)
+        gd, gi = B.ivfpq_search(wi.index, _t(q), 64, 100)
+        torch.cuda.synchronize()
+    finally:
+        B.ivfpq_set_lut_type(wi.index, "fp32")
+    gp, gi = gp.cpu().numpy(), gi.cpu().numpy()
     rows = np.random.default_rng(4).choice(w.nq, 256, replace=False)
-    _, oi, _ = oracle.ivfpq_search(q[rows], data.cent, data.cb, data.list_off, data.codes,
-                                   data.ids, 64, 100, forced_probes=gp[rows])
+    codes_h, lists_h, ids_h = indexing.lists_on_host(wi, np.unique(gp[rows]))
+    off, codes_l, ids_l = oracle.to_lists(codes_h, lists_h, ids_h, wi.cent.shape[0])
+    _, oi, _ = oracle.ivfpq_search(q[rows], wi.cent, wi.codebooks.cpu().numpy(), off, codes_l,
+                                   ids_l, 64, 100, forced_probes=gp[rows])
     r = oracle.recall_at_k(gi[rows], oi)
     print(f"{lut} recall@100 vs fp32 oracle = {r:.4f}")
     assert r >= gate
-    torch.cuda.empty_cache()
 
 
 @pytest.mark.parametrize("k", [10, 40])
