@@ -44,6 +44,7 @@ SIGNATURES = {
     "ivfpq_stage_times": (_I, [_VP, C.POINTER(C.c_float), C.POINTER(C.c_int)]),
     "ivfpq_last_scan_kernel": (C.c_char_p, [_VP]),
     "ivfpq_set_precomputed": (_I, [_VP, _I]),
+    "ivfpq_set_scan_mode": (_I, [_VP, _I, _I]),
     "ivfpq_uses_precomputed": (_I, [_VP]),
     "ivfpq_kernel_launches": (C.c_uint64, []),
     "flat_knn": (_I, [_VP, _I64, _I, _VP, _I64, _I, _VP, _VP, _VP]),
@@ -294,6 +295,12 @@ def ivfpq_set_precomputed(index, mode):
     lookup tables; returns whether searches now use them."""
     _check("ivfpq_set_precomputed", lib().ivfpq_set_precomputed(index.handle, int(mode)))
     return bool(lib().ivfpq_uses_precomputed(index.handle))
+
+
+def ivfpq_set_scan_mode(index, mode, group=0):
+    """-1 automatic, 0 by query, 1 by list (where its shapes apply); group =
+    queries per table set of the by-list scan (2 or 3; 0 keeps it)."""
+    _check("ivfpq_set_scan_mode", lib().ivfpq_set_scan_mode(index.handle, int(mode), int(group)))
 
 
 def ivfpq_uses_precomputed(index):

@@ -100,7 +100,7 @@ class Workspace {
   }
 
  private:
-  static const int kMax = 16;
+  static const int kMax = 32;
   cudaStream_t s_;
   void* p_[kMax];
   int n_ = 0;

@@ -137,6 +137,10 @@ struct ivfpq_index {
   // tables are in use (precomputed: -1 automatic, 0 off, 1 on)
   float* term1 = nullptr;
   int precomputed = -1;
+  // list scan organisation: -1 automatic, 0 by query, 1 by list (list-major,
+  // where its shapes apply); the queries per list sharing one table set
+  int scan_mode = -1;
+  int lm_group = 3;
   // tensor-core operands of the centroids (null when that path is unavailable)
   float* cent_hi = nullptr;     // [nlist, tc_dpad(d)]
   float* cent_lo = nullptr;

@@ -7,10 +7,13 @@
 // per query x list, queries x lists processed independently, two-pass
 // k-selection with subdivision factor f: here f = the number of list chunks
 // per query).
+#include <cub/cub.cuh>
+
 #include <algorithm>
 
 #include "internal.h"
 #include "scan2.cuh"
+#include "scan_lm.cuh"
 
 namespace ivfpq {
 
@@ -64,6 +67,36 @@ int try_scan2_kw(const ScanParams& p, int64_t nq, cudaStream_t s, int* launched)
                  : launch_scan2<2, 12, KW, false>(p, nq, s);
     case 808:
       return pre ? launch_scan2<2, 8, KW, true>(p, nq, s) : launch_scan2<2, 8, KW, false>(p, nq, s);
+  }
+  *launched = 0;
+  return IVFPQ_OK;
+}
+
+#define IVFPQ_EXTERN_SCAN_LM(MW, DS)                                                     \
+  extern template int launch_scan_lm<MW, DS, 2, 0>(const LmParams&, cudaStream_t);     \
+  extern template int launch_scan_lm<MW, DS, 3, 0>(const LmParams&, cudaStream_t);     \
+  extern template int launch_scan_lm<MW, DS, 1, 2>(const LmParams&, cudaStream_t);     \
+  extern template int launch_scan_lm<MW, DS, 1, 4>(const LmParams&, cudaStream_t);     \
+  extern template int launch_scan_lm<MW, DS, 1, 8>(const LmParams&, cudaStream_t);
+IVFPQ_EXTERN_SCAN_LM(8, 3)
+IVFPQ_EXTERN_SCAN_LM(8, 4)
+IVFPQ_EXTERN_SCAN_LM(4, 8)
+IVFPQ_EXTERN_SCAN_LM(4, 4)
+IVFPQ_EXTERN_SCAN_LM(2, 12)
+IVFPQ_EXTERN_SCAN_LM(2, 8)
+
+// The list-major kernel (scan_lm.cuh): the filter pass with G queries per
+// table set (TQ = 0) or the bound pass with TQ-entry lane queues (G = 1).
+template <int G, int KW>
+int try_scan_lm(const LmParams& p, cudaStream_t s, int* launched) {
+  *launched = 1;
+  switch (p.s.m * 100 + p.s.dsub) {
+    case 3203: return launch_scan_lm<8, 3, G, KW>(p, s);
+    case 3204: return launch_scan_lm<8, 4, G, KW>(p, s);
+    case 1608: return launch_scan_lm<4, 8, G, KW>(p, s);
+    case 1604: return launch_scan_lm<4, 4, G, KW>(p, s);
+    case 812: return launch_scan_lm<2, 12, G, KW>(p, s);
+    case 808: return launch_scan_lm<2, 8, G, KW>(p, s);
   }
   *launched = 0;
   return IVFPQ_OK;
@@ -135,6 +168,15 @@ __global__ void warp_queue_check_kernel(const uint32_t* __restrict__ pkeys, int6
   if ((threadIdx.x & 31) == 0 && c) atomicAdd(repaired, (unsigned long long)c);
 }
 
+// *repaired += number of flagged queries
+__global__ void count_flags_kernel(const int* __restrict__ flags, int64_t nq,
+                                   unsigned long long* __restrict__ repaired) {
+  const int64_t q = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int f = q < nq ? flags[q] : 0;
+  const unsigned c = __popc(__ballot_sync(kFullMask, f != 0));
+  if ((threadIdx.x & 31) == 0 && c) atomicAdd(repaired, (unsigned long long)c);
+}
+
 const size_t kMaxEventSets = 4096;
 
 // Starts a new event set for this search (profiling only).
@@ -154,6 +196,177 @@ void record(const ivfpq_index* ix, int i, cudaStream_t s) {
   auto& set = mix->ev_sets[mix->cur_set];
   if (!set.ev[i] && cudaEventCreate(&set.ev[i]) != cudaSuccess) return;
   if (cudaEventRecord(set.ev[i], s) == cudaSuccess) set.recorded[i] = true;
+}
+
+// ---- list-major scan: planning and final selection ----------------------------
+
+// Record of every item (one warp per item): its list, length, first block,
+// queries and their bounds (the sentinel in the bound pass), and the
+// residual of each of its queries to the list's centroid.
+__global__ void lm_records_kernel(const LmParams p, int G, bool bound_pass, uint8_t* records) {
+  const ScanParams& sp = p.s;
+  const int lane = threadIdx.x & 31;
+  const int nit = *p.n_items;
+  const int warps = int(gridDim.x) * (blockDim.x >> 5);
+  for (int it = int(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); it < nit; it += warps) {
+    const int64_t pos = p.items[it];
+    const int l = p.pair_list[pos];
+    const bool mine = lane < G && pos + lane < p.npairs && p.pair_list[pos + lane] == l;
+    const unsigned vm = __ballot_sync(kFullMask, mine);
+    const int nq = __popc(vm);
+    uint8_t* rec = records + int64_t(it) * p.rec_bytes;
+    LmHead* h = reinterpret_cast<LmHead*>(rec);
+    int qv = 0;
+    if (mine) {
+      qv = p.pair_query[pos + lane];
+      h->q[lane] = qv;
+      h->theta[lane] = bound_pass ? kSentinelKey : p.theta_key[int64_t(qv) * p.theta_stride];
+    }
+    if (lane == 0) {
+      h->list = l;
+      h->nq = nq;
+      h->len = sp.list_len[l];
+      h->boff = sp.list_block_off[l];
+    }
+    float* res = reinterpret_cast<float*>(rec + kLmHead);
+    const float* c = sp.centroids + int64_t(l) * sp.d;
+    for (int g = 0; g < nq; ++g) {
+      const int qg = __shfl_sync(kFullMask, qv, g);
+      const float* x = sp.queries + int64_t(qg) * sp.d;
+      for (int t = lane; t < p.dpad; t += 32) res[g * p.dpad + t] = t < sp.d ? x[t] - c[t] : 0.f;
+    }
+  }
+}
+
+
+// probes[q][col] -> out[q]
+__global__ void probe_column_kernel(const int32_t* __restrict__ probes, int64_t nq, int nprobe,
+                                    int col, int32_t* __restrict__ out) {
+  const int64_t q = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (q < nq) out[q] = probes[q * nprobe + col];
+}
+
+// (list, query) pairs of probes p0 .. p0 + per - 1; a list id outside
+// [0, nlist) becomes nlist (sorted last, no item)
+__global__ void lm_pairs_kernel(const int32_t* __restrict__ probes, int64_t nq, int nprobe,
+                                int p0, int per, int nlist, int32_t* __restrict__ key,
+                                int32_t* __restrict__ val) {
+  const int64_t n = nq * per;
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t q = i / per;
+    const int l = probes[q * nprobe + p0 + (i - q * per)];
+    key[i] = (l >= 0 && l < nlist) ? l : nlist;
+    val[i] = int32_t(q);
+  }
+}
+
+// flag[i] = 1 where sorted pair i starts an item: its rank among the pairs
+// of its list is a multiple of G (rank from a binary search for the list's
+// first pair)
+__global__ void lm_item_flags_kernel(const int32_t* __restrict__ skey, int64_t n, int G,
+                                     int nlist, int32_t* __restrict__ flag) {
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int32_t l = skey[i];
+    int64_t lo = 0, hi = i;  // first index with skey == l lies in [lo, hi]
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (skey[mid] < l) lo = mid + 1;
+      else hi = mid;
+    }
+    flag[i] = (l < nlist && (i - lo) % G == 0) ? 1 : 0;
+  }
+}
+
+// items[pos[i]] = i for the flagged pairs; *n_items = their number
+__global__ void lm_items_kernel(const int32_t* __restrict__ flag, const int32_t* __restrict__ pos,
+                                int64_t n, int32_t* __restrict__ items, int* __restrict__ n_items) {
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    if (flag[i]) items[pos[i]] = int32_t(i);
+    if (i == n - 1) *n_items = pos[i] + flag[i];
+  }
+}
+
+// theta[r] = the k-th smallest of row r's len keys (the sentinel when fewer
+// than k keys are below it): one warp per row, a binary search over the
+// 32-bit key range for the least v with at least k keys <= v.
+__global__ void lm_theta_kernel(const uint32_t* __restrict__ keys, int64_t rows, int len, int k,
+                                uint32_t* __restrict__ theta) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;  // the same for the whole warp
+  const uint32_t* kr = keys + row * len;
+  uint32_t lo = 0, hi = kSentinelKey;
+  while (lo < hi) {
+    const uint32_t mid = lo + ((hi - lo) >> 1);
+    int c = 0;
+    for (int i = lane; i < len; i += 32) c += kr[i] <= mid ? 1 : 0;
+#pragma unroll
+    for (int o = 16; o >= 1; o /= 2) c += __shfl_xor_sync(kFullMask, c, o);
+    if (c >= k) hi = mid;
+    else lo = mid + 1;
+  }
+  if (lane == 0) theta[row] = lo;
+}
+
+// The k smallest of a query's nearest-list result (k entries, ascending,
+// (+inf, -1) padded) and its candidates from the other lists; one block per
+// query, a bitonic sort of the <= k + cap entries in shared memory. A query
+// whose candidates overflowed the buffer is flagged for the full rescan.
+__global__ void lm_final_kernel(const float* __restrict__ pre_d, const int64_t* __restrict__ pre_i,
+                                int k, const uint32_t* __restrict__ ckey,
+                                const int64_t* __restrict__ cid, const int* __restrict__ ccount,
+                                int cap, float* __restrict__ out_d, int64_t* __restrict__ out_i,
+                                int* __restrict__ flags) {
+  extern __shared__ uint32_t lmf_smem[];
+  const int64_t q = blockIdx.x;
+  const int cnt = ccount[q];
+  const int n2 = min(cnt, cap);
+  const int total = k + n2;
+  int T = 32;
+  while (T < total) T *= 2;
+  uint32_t* sk = lmf_smem;
+  uint32_t* sv = lmf_smem + T;
+  for (int i = threadIdx.x; i < T; i += blockDim.x) {
+    uint32_t key = kSentinelKey;
+    if (i < k) {
+      if (pre_i && pre_i[q * k + i] >= 0) key = __float_as_uint(pre_d[q * k + i]);
+    } else if (i < total) {
+      key = ckey[q * cap + (i - k)];
+    }
+    sk[i] = key;
+    sv[i] = uint32_t(i);
+  }
+  __syncthreads();
+  for (int size = 2; size <= T; size *= 2) {
+    for (int st = size / 2; st >= 1; st /= 2) {
+      for (int c = threadIdx.x; c < T / 2; c += blockDim.x) {
+        const int lo = 2 * c - (c & (st - 1));
+        const int hi = lo + st;
+        const bool up = (lo & size) == 0;
+        const uint32_t a = sk[lo], b = sk[hi];
+        if ((a > b) == up) {
+          sk[lo] = b;
+          sk[hi] = a;
+          const uint32_t t = sv[lo];
+          sv[lo] = sv[hi];
+          sv[hi] = t;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = threadIdx.x; i < k; i += blockDim.x) {
+    const uint32_t key = sk[i];
+    const uint32_t src = sv[i];
+    out_d[q * k + i] = dist_key_to_float(key);
+    out_i[q * k + i] = key == kSentinelKey ? int64_t(-1)
+                       : src < uint32_t(k) ? pre_i[q * k + src]
+                                           : cid[q * cap + (src - k)];
+  }
+  if (threadIdx.x == 0) flags[q] = cnt > cap ? 1 : 0;
 }
 
 int coarse_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int nprobe,
@@ -179,8 +392,8 @@ void plan_chunks(int64_t nq, int nprobe, int* per_chunk, int* nchunks) {
   *nchunks = int(ceil_div(nprobe, pc));
 }
 
-int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int nprobe,
-               const int32_t* probes, int k, float* out_dist, int64_t* out_ids, cudaStream_t s) {
+ScanParams scan_params(const ivfpq_index* ix, const float* queries, int64_t nq, int nprobe,
+                       const int32_t* probes, int k) {
   ScanParams p;
   p.queries = queries;
   p.centroids = ix->centroids;
@@ -197,8 +410,34 @@ int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int npro
   p.nprobe = nprobe;
   p.k = k;
   p.lut_type = ix->lut_type;
-  if (use_precomputed(ix)) p.term1 = ix->term1;
   plan_chunks(nq, nprobe, &p.per_chunk, &p.nchunks);
+  return p;
+}
+
+// Re-scans, with the general kernel and full-length queues, the queries
+// flagged in `flags` (device, [nq]) and overwrites their results.
+int repair_stage(const ScanParams& p0, int64_t nq, int* flags, const SelectOut& o, Workspace& ws,
+                 cudaStream_t s) {
+  ScanParams r = p0;
+  r.term1 = nullptr;
+  plan_chunks(nq, r.nprobe, &r.per_chunk, &r.nchunks);
+  r.qmask = flags;
+  const size_t nr = size_t(nq) * r.nchunks * r.k;
+  IVFPQ_TRY(ws.alloc(&r.pkeys, nr));
+  IVFPQ_TRY(ws.alloc(&r.pidx, nr));
+  IVFPQ_TRY(launch_scan_general(r, nq, s));
+  SelectOut ro = o;
+  ro.row_mask = flags;
+  const int64_t rlen = int64_t(r.nchunks) * r.k;
+  return select_pairs(r.pkeys, r.pidx, nq, rlen, r.k, 1, rlen, ro, s);
+}
+
+// The list scan organised by query: one block per (query, chunk of lists).
+int scan_stage_qm(const ivfpq_index* ix, const float* queries, int64_t nq, int nprobe,
+                  const int32_t* probes, int k, float* out_dist, int64_t* out_ids,
+                  cudaStream_t s, bool timed) {
+  ScanParams p = scan_params(ix, queries, nq, nprobe, probes, k);
+  if (use_precomputed(ix)) p.term1 = ix->term1;
   Workspace ws(s);
   SelectOut o;
   o.kind = OutKind::Dist;
@@ -210,13 +449,13 @@ int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int npro
     const size_t np = size_t(nq) * p.nchunks * k;
     IVFPQ_TRY(ws.alloc(&p.pkeys, np));
     IVFPQ_TRY(ws.alloc(&p.pidx, np));
-    record(ix, 2, s);
+    if (timed) record(ix, 2, s);
     IVFPQ_TRY(launch_scan_general(p, nq, s));
     mix->last_scan_kernel.store("ivfpq_scan_kernel");
-    record(ix, 3, s);
+    if (timed) record(ix, 3, s);
     const int64_t len = int64_t(p.nchunks) * k;
     IVFPQ_TRY(select_pairs(p.pkeys, p.pidx, nq, len, k, 1, len, o, s));
-    record(ix, 4, s);
+    if (timed) record(ix, 4, s);
     return IVFPQ_OK;
   }
   // register-codebook kernel: per-warp queues of kw entries, unmerged; at
@@ -230,7 +469,7 @@ int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int npro
   const size_t np = size_t(nq) * groups * kw;
   IVFPQ_TRY(ws.alloc(&p.pkeys, np));
   IVFPQ_TRY(ws.alloc(&p.pidx, np));
-  record(ix, 2, s);
+  if (timed) record(ix, 2, s);
   int launched = 0;
   switch (kw) {
     case 32: IVFPQ_TRY(try_scan2_kw<32>(p, nq, s, &launched)); break;
@@ -240,7 +479,7 @@ int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int npro
   }
   IVFPQ_REQUIRE(launched, "scan: no register-codebook kernel for m=%d d/m=%d", p.m, p.dsub);
   mix->last_scan_kernel.store("ivfpq_scan2_kernel");
-  record(ix, 3, s);
+  if (timed) record(ix, 3, s);
   IVFPQ_TRY(merge_sorted_runs(p.pkeys, p.pidx, nq, groups, kw, k, o, s));
   if (kw < k) {
     // repair the queries whose merged result a short queue may have cut
@@ -249,19 +488,169 @@ int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int npro
     warp_queue_check_kernel<<<unsigned(ceil_div(nq, 256)), 256, 0, s>>>(
         p.pkeys, nq, groups, kw, out_dist, k, flags, ix->repaired);
     IVFPQ_LAUNCHED();
-    ScanParams r = p;
-    r.qmask = flags;
-    const size_t nr = size_t(nq) * p.nchunks * k;
-    IVFPQ_TRY(ws.alloc(&r.pkeys, nr));
-    IVFPQ_TRY(ws.alloc(&r.pidx, nr));
-    IVFPQ_TRY(launch_scan_general(r, nq, s));
-    SelectOut ro = o;
-    ro.row_mask = flags;
-    const int64_t rlen = int64_t(p.nchunks) * k;
-    IVFPQ_TRY(select_pairs(r.pkeys, r.pidx, nq, rlen, k, 1, rlen, ro, s));
+    IVFPQ_TRY(repair_stage(p, nq, flags, o, ws, s));
   }
+  if (timed) record(ix, 4, s);
+  return IVFPQ_OK;
+}
+
+// Whether a search takes the list-major scan: its shapes (as the
+// register-codebook scan, fp32 tables, direct tables), at least two probes,
+// and (automatic mode) on average at least two queries per probed list.
+bool use_list_major(const ivfpq_index* ix, int64_t nq, int nprobe) {
+  if (ix->scan_mode == 0 || nprobe < 2 || nq < 1 || ix->precomputed == 1) return false;
+  ScanParams p;
+  p.m = ix->m;
+  p.dsub = ix->dsub;
+  p.d = ix->d;
+  p.k = 1;
+  p.lut_type = ix->lut_type;
+  if (!scan2_shape(p)) return false;
+  if (ix->scan_mode == 1) return true;
+  return double(nq) * nprobe >= 2.0 * ix->nlist;
+}
+
+// (list, query) pairs of probes [p0, p0 + per) sorted by list and cut into
+// items of up to G pairs of one list (into lp's pair and item arrays).
+int plan_items(const int32_t* probes, int64_t nq, int nprobe, int p0, int per, int G, int nlist,
+               Workspace& ws, cudaStream_t s, LmParams& lp) {
+  const int64_t npairs = nq * per;
+  IVFPQ_REQUIRE(npairs < (int64_t(1) << 31), "scan: %lld (list, query) pairs", (long long)npairs);
+  int32_t *key = nullptr, *val = nullptr, *skey = nullptr, *sval = nullptr;
+  int32_t *flag = nullptr, *pos = nullptr, *items = nullptr;
+  int* n_items = nullptr;
+  IVFPQ_TRY(ws.alloc(&key, size_t(npairs)));
+  IVFPQ_TRY(ws.alloc(&val, size_t(npairs)));
+  IVFPQ_TRY(ws.alloc(&skey, size_t(npairs)));
+  IVFPQ_TRY(ws.alloc(&sval, size_t(npairs)));
+  IVFPQ_TRY(ws.alloc(&flag, size_t(npairs)));
+  IVFPQ_TRY(ws.alloc(&pos, size_t(npairs)));
+  IVFPQ_TRY(ws.alloc(&items, size_t(npairs)));
+  IVFPQ_TRY(ws.alloc(&n_items, 1));
+  const unsigned pg = unsigned(std::max<int64_t>(1, std::min<int64_t>(ceil_div(npairs, 256),
+                                                                    int64_t(num_sms()) * 16)));
+  lm_pairs_kernel<<<pg, 256, 0, s>>>(probes, nq, nprobe, p0, per, nlist, key, val);
+  IVFPQ_LAUNCHED();
+  int end_bit = 1;
+  while ((int64_t(1) << end_bit) <= nlist) ++end_bit;
+  size_t sort_bytes = 0, scan_bytes = 0;
+  IVFPQ_CUDA(cub::DeviceRadixSort::SortPairs(nullptr, sort_bytes, key, skey, val, sval, npairs, 0,
+                                             end_bit, s));
+  IVFPQ_CUDA(cub::DeviceScan::ExclusiveSum(nullptr, scan_bytes, flag, pos, npairs, s));
+  uint8_t* tmp = nullptr;
+  IVFPQ_TRY(ws.alloc(&tmp, std::max(sort_bytes, scan_bytes)));
+  IVFPQ_CUDA(cub::DeviceRadixSort::SortPairs(tmp, sort_bytes, key, skey, val, sval, npairs, 0,
+                                             end_bit, s));
+  lm_item_flags_kernel<<<pg, 256, 0, s>>>(skey, npairs, G, nlist, flag);
+  IVFPQ_LAUNCHED();
+  IVFPQ_CUDA(cub::DeviceScan::ExclusiveSum(tmp, scan_bytes, flag, pos, npairs, s));
+  lm_items_kernel<<<pg, 256, 0, s>>>(flag, pos, npairs, items, n_items);
+  IVFPQ_LAUNCHED();
+  lp.pair_list = skey;
+  lp.pair_query = sval;
+  lp.items = items;
+  lp.n_items = n_items;
+  lp.npairs = npairs;
+  return IVFPQ_OK;
+}
+
+// Item records (scan_lm.cuh, lm_records_kernel) for the items of lp, after
+// lp's bounds are set; room for one record per pair (the item count stays on
+// the device).
+int make_records(LmParams& lp, int G, bool bound_pass, Workspace& ws, cudaStream_t s) {
+  lp.dpad = (lp.s.d + 3) & ~3;
+  lp.rec_bytes = lm_record_bytes(G, lp.s.d);
+  uint8_t* rec = nullptr;
+  IVFPQ_TRY(ws.alloc(&rec, size_t(std::max<int64_t>(lp.npairs, 1)) * lp.rec_bytes));
+  const unsigned rg = unsigned(std::max<int64_t>(
+      1, std::min<int64_t>(ceil_div(lp.npairs, 8), int64_t(num_sms()) * 16)));
+  lm_records_kernel<<<rg, 256, 0, s>>>(lp, G, bound_pass, rec);
+  IVFPQ_LAUNCHED();
+  lp.records = rec;
+  return IVFPQ_OK;
+}
+
+// The list scan organised by list (scan_lm.cuh): a bound pass over every
+// query's nearest list, a filter pass over all its lists, one selection per
+// query over its candidates, and the full rescan of queries whose candidates
+// overflowed.
+int scan_stage_lm(const ivfpq_index* ix, const float* queries, int64_t nq, int nprobe,
+                  const int32_t* probes, int k, float* out_dist, int64_t* out_ids,
+                  cudaStream_t s) {
+  auto* mix = const_cast<ivfpq_index*>(ix);
+  Workspace ws(s);
+  record(ix, 2, s);
+  const ScanParams base = scan_params(ix, queries, nq, nprobe, probes, k);
+  // 1. bound pass: per query, 512 lane queues of tq over its nearest list
+  //    (512 * tq >= 2k), and the k-th smallest of their entries
+  const int tq = k <= 512 ? 2 : k <= 1024 ? 4 : 8;
+  LmParams bp;
+  bp.s = base;
+  IVFPQ_TRY(plan_items(probes, nq, nprobe, 0, 1, 1, ix->nlist, ws, s, bp));
+  IVFPQ_TRY(make_records(bp, 1, true, ws, s));
+  const int64_t plen = int64_t(kLmWarps) * 32 * tq;
+  const size_t npart = size_t(nq) * plen;
+  IVFPQ_TRY(ws.alloc(&bp.part_key, npart));
+  IVFPQ_CUDA(cudaMemsetAsync(bp.part_key, 0xff, npart * sizeof(uint32_t), s));
+  int launched = 0;
+  switch (tq) {
+    case 2: IVFPQ_TRY((try_scan_lm<1, 2>(bp, s, &launched))); break;
+    case 4: IVFPQ_TRY((try_scan_lm<1, 4>(bp, s, &launched))); break;
+    default: IVFPQ_TRY((try_scan_lm<1, 8>(bp, s, &launched))); break;
+  }
+  IVFPQ_REQUIRE(launched, "scan: no list-major kernel for m=%d d/m=%d", ix->m, ix->dsub);
+  uint32_t* theta = nullptr;
+  IVFPQ_TRY(ws.alloc(&theta, size_t(nq)));
+  lm_theta_kernel<<<unsigned(ceil_div(nq, 8)), 256, 0, s>>>(bp.part_key, nq, int(plen), k, theta);
+  IVFPQ_LAUNCHED();
+  // 2. filter pass over all the probed lists
+  LmParams lp;
+  lp.s = base;
+  const int G = ix->lm_group;
+  IVFPQ_TRY(plan_items(probes, nq, nprobe, 0, nprobe, G, ix->nlist, ws, s, lp));
+  const int cap = std::max(1024, 2 * k);
+  lp.theta_key = theta;
+  lp.theta_stride = 1;
+  lp.ids = ix->ids;
+  lp.cap = cap;
+  IVFPQ_TRY(make_records(lp, G >= 3 ? 3 : 2, false, ws, s));
+  IVFPQ_TRY(ws.alloc(&lp.ckey, size_t(nq) * cap));
+  IVFPQ_TRY(ws.alloc(&lp.cid, size_t(nq) * cap));
+  IVFPQ_TRY(ws.alloc(&lp.ccount, size_t(nq)));
+  IVFPQ_CUDA(cudaMemsetAsync(lp.ccount, 0, size_t(nq) * sizeof(int), s));
+  if (G >= 3) IVFPQ_TRY((try_scan_lm<3, 0>(lp, s, &launched)));
+  else IVFPQ_TRY((try_scan_lm<2, 0>(lp, s, &launched)));
+  IVFPQ_REQUIRE(launched, "scan: no list-major kernel for m=%d d/m=%d", ix->m, ix->dsub);
+  mix->last_scan_kernel.store("ivfpq_scan_lm_kernel");
+  record(ix, 3, s);
+  // 3. the k smallest candidates of each query
+  int* flags = nullptr;
+  IVFPQ_TRY(ws.alloc(&flags, size_t(nq)));
+  int T = 32;
+  while (T < k + cap) T *= 2;
+  const size_t fsm = size_t(T) * 8;
+  IVFPQ_TRY(set_dynamic_smem(lm_final_kernel, fsm));
+  lm_final_kernel<<<unsigned(nq), 256, fsm, s>>>(nullptr, nullptr, k, lp.ckey, lp.cid, lp.ccount,
+                                                 cap, out_dist, out_ids, flags);
+  IVFPQ_LAUNCHED_K(lm_final_kernel, fsm, 256);
+  // 4. queries whose candidates overflowed: full rescan
+  count_flags_kernel<<<unsigned(ceil_div(nq, 256)), 256, 0, s>>>(flags, nq, ix->repaired);
+  IVFPQ_LAUNCHED();
+  SelectOut o;
+  o.kind = OutKind::Dist;
+  o.vals = out_dist;
+  o.idx64 = out_ids;
+  o.id_map = ix->ids;
+  IVFPQ_TRY(repair_stage(base, nq, flags, o, ws, s));
   record(ix, 4, s);
   return IVFPQ_OK;
+}
+
+int scan_stage(const ivfpq_index* ix, const float* queries, int64_t nq, int nprobe,
+               const int32_t* probes, int k, float* out_dist, int64_t* out_ids, cudaStream_t s) {
+  if (use_list_major(ix, nq, nprobe))
+    return scan_stage_lm(ix, queries, nq, nprobe, probes, k, out_dist, out_ids, s);
+  return scan_stage_qm(ix, queries, nq, nprobe, probes, k, out_dist, out_ids, s, true);
 }
 
 int check_common(const ivfpq_index* ix, const float* queries, int64_t nq, int nprobe,
@@ -395,6 +784,17 @@ extern "C" int ivfpq_set_profiling(ivfpq_index* ix, int enable) {
   ix->profile = enable != 0;
   ix->ev_used = 0;
   ix->cur_set = -1;
+  return IVFPQ_OK;
+}
+
+extern "C" int ivfpq_set_scan_mode(ivfpq_index* ix, int mode, int group) {
+  clear_error();
+  IVFPQ_REQUIRE(ix, "ivfpq_set_scan_mode: null index");
+  IVFPQ_REQUIRE(mode >= -1 && mode <= 1, "ivfpq_set_scan_mode: mode=%d outside [-1, 1]", mode);
+  IVFPQ_REQUIRE(group == 0 || group == 2 || group == 3,
+                "ivfpq_set_scan_mode: group=%d (0 keeps the current, else 2 or 3)", group);
+  ix->scan_mode = mode;
+  if (group) ix->lm_group = group;
   return IVFPQ_OK;
 }
 

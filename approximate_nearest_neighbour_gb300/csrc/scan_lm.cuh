@@ -1,0 +1,355 @@
+// List-major ADC scan: the queries that probe one inverted list are scanned
+// together, so one load of a code block and one byte permute per code byte
+// serve the tables of G queries.
+//
+// Same computation as the other list scans ("Billion-scale similarity search
+// with GPUs", section 5: tables T_1..T_b per query and list, b look-ups and
+// additions per code; "Custom 8-bit floating point value format ...", search
+// steps 2-5 and Eq. (1)); the section's queries x lists work is organised by
+// list instead of by query:
+//  * a work item is one list and up to G of the queries that probe it (the
+//    (list, query) pairs sorted by list, cut into groups of G); items run in
+//    list order, so the blocks working at one time share lists in L2;
+//  * one persistent block of 16 warps per SM takes items blockIdx.x,
+//    blockIdx.x + gridDim.x, ...; the 256 x m codewords stay in registers
+//    for the whole kernel (d/2 floats per thread, as in scan2.cuh);
+//  * shared memory holds G table sets, each a 256 x 64-word array whose two
+//    32-column halves are the double buffer: item t is scanned from half
+//    t & 1 while item t + 1's tables are built into the other half; a
+//    column c of a half holds table c mod m, lane i reads column
+//    (i & ~(m-1)) | ((i + s) & (m-1)) at stored position s (table
+//    (i + s) mod m, the sub-quantizer of that stored byte), so the 32 lanes
+//    of a look-up hit 32 banks; the query and the half are immediates;
+//  * selection is a filter: every query has a bound theta, and a code whose
+//    distance is at most theta is appended, with its id, to the query's
+//    candidate buffer (one atomic per warp and query); the k smallest
+//    candidates are the query's result, and a query whose buffer overflows
+//    is scanned again by the general kernel;
+//  * the bound comes from a first pass of the same kernel over every query's
+//    nearest list alone (one query per item, TQ > 0): each lane keeps the TQ
+//    smallest distances of the codes it scores (a sorted register queue, no
+//    communication between lanes) and writes them out; the k-th smallest of
+//    those 512 * TQ distances (512 * TQ >= k) is at least the k-th smallest
+//    of the list (a lane that saw more than TQ of the list's k smallest only
+//    makes it larger), hence at least the query's final k-th distance.
+#pragma once
+
+#include <type_traits>
+
+#include "scan2.cuh"
+
+namespace ivfpq {
+
+constexpr int kLmWarps = 16;
+constexpr int kLmSlots = 3;  // item descriptors in flight: scanned, built, fetched
+
+struct LmParams {
+  ScanParams s;                // tables, lists, codes, shapes (nprobe unused)
+  const int32_t* pair_list;    // [npairs] list of each (list, query) pair, sorted
+  const int32_t* pair_query;   // [npairs] query of each pair
+  const int32_t* items;        // [n_items] first pair of each item
+  const int* n_items;          // device scalar
+  int64_t npairs;
+  // filter pass: bound of query q (raw bits of a distance >= 0, or the
+  // sentinel for none) at theta_key[q * theta_stride]
+  const uint32_t* theta_key;
+  int theta_stride;
+  const int64_t* ids;          // slot -> id
+  uint32_t* ckey;              // [nq, cap] candidate distances (raw bits)
+  int64_t* cid;                // [nq, cap] candidate ids
+  int* ccount;                 // [nq] candidates appended (may exceed cap)
+  int cap;
+  // bound pass: lane i of warp w's TQ smallest distances for query q at
+  // part_key[((q * 16 + w) * 32 + i) * TQ ..], ascending, sentinel-padded
+  uint32_t* part_key;
+  // item records (lm_records_kernel): rec_bytes each
+  const uint8_t* records;
+  int rec_bytes;
+  int dpad;                    // d rounded up to a multiple of 4
+};
+
+// Head of an item record; the G residuals x_q - c_list (dpad floats each)
+// follow at byte kLmHead.
+struct LmHead {
+  int list, len, nq, pad;
+  int64_t boff;
+  int q[3];
+  uint32_t theta[3];
+};
+constexpr int kLmHead = 64;
+static_assert(sizeof(LmHead) <= kLmHead, "record head");
+
+inline int lm_record_bytes(int G, int d) { return kLmHead + G * ((d + 3) & ~3) * 4; }
+
+__device__ __forceinline__ void lm_cp_async16(void* smem, const void* gmem) {
+  const uint32_t sa = uint32_t(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+// Column byte offsets of stored positions 4a .. 4a + 3 for lane `lane`, one
+// per byte (each below 128).
+template <int GS>
+__device__ __forceinline__ uint32_t lm_lane_columns(int lane, int a) {
+  uint32_t r = 0;
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    const int s = 4 * a + b;
+    const uint32_t c = uint32_t((lane & ~(GS - 1)) | ((lane + s) & (GS - 1)));
+    r |= (c * 4u) << (8 * b);
+  }
+  return r;
+}
+
+template <int SEL>
+__device__ __forceinline__ uint32_t lm_prmt(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "n"(SEL));
+  return r;
+}
+
+// Table look-ups of one slot for GG queries: acc[g][s & 3] += T_g[row(s)][col(s)]
+// for every stored position s. The row is code byte s & 3 of word s / 4,
+// the column byte offset byte s & 3 of lcol[s / 4]; one prmt puts them at
+// bytes 1 and 0 (its two upper bytes are copies of the sign of a column
+// byte, zero). Table set g of half P is at byte g * 65536 + 128 * P.
+template <int MW, int GG, int P, int S = 0>
+__device__ __forceinline__ void lm_lookups(const uint32_t (&w)[MW], const char* tab,
+                                           const uint32_t (&lcol)[MW], float (&acc)[GG][4]) {
+  if constexpr (S < 4 * MW) {
+    constexpr int SEL = 0xCC00 | ((S & 3) << 4) | (4 + (S & 3));
+    const uint32_t off = lm_prmt<SEL>(w[S >> 2], lcol[S >> 2]);
+#pragma unroll
+    for (int g = 0; g < GG; ++g)
+      acc[g][S & 3] += *reinterpret_cast<const float*>(tab + off + g * 65536 + 128 * P);
+    lm_lookups<MW, GG, P, S + 1>(w, tab, lcol, acc);
+  }
+}
+
+// Appends (dist, id of slot) to query q's candidates where `pass` holds.
+// All 32 lanes call it together.
+__device__ __forceinline__ void lm_append(const LmParams& p, int q, bool pass, float dist,
+                                          uint32_t slot, int lane) {
+  const unsigned mask = __ballot_sync(kFullMask, pass);
+  if (mask == 0u) return;
+  const int leader = __ffs(mask) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(p.ccount + q, __popc(mask));
+  base = __shfl_sync(kFullMask, base, leader);
+  if (pass) {
+    const int pos = base + __popc(mask & ((1u << lane) - 1u));
+    if (pos < p.cap) {
+      const int64_t o = int64_t(q) * p.cap + pos;
+      p.ckey[o] = __float_as_uint(dist);
+      p.cid[o] = p.ids[slot];
+    }
+  }
+}
+
+template <int MW, int DS, int G, int TQ>
+__global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const LmParams p) {
+  static_assert(TQ == 0 || G == 1, "the bound pass takes one query per item");
+  using Sh = Scan2Shape<MW, DS>;
+  constexpr int NW = kLmWarps;
+  constexpr int m = Sh::M;
+  constexpr int GS = Sh::GS;
+  constexpr int QQ = 32 / GS;
+  constexpr int STEPS = 256 / (NW * QQ);
+  constexpr int REPS = 32 / GS;
+  static_assert(kScan2Warps == NW, "codeword ownership as in scan2.cuh");
+  extern __shared__ __align__(16) uint32_t lm_smem[];
+  float* tab = reinterpret_cast<float*>(lm_smem);  // G x [256][64] fp32
+  uint8_t* slots = reinterpret_cast<uint8_t*>(lm_smem + G * kGroupWords);
+  auto head = [&](int slot) -> const LmHead& {
+    return *reinterpret_cast<const LmHead*>(slots + slot * p.rec_bytes);
+  };
+  auto resid = [&](int slot) {
+    return reinterpret_cast<const float*>(slots + slot * p.rec_bytes + kLmHead);
+  };
+  const ScanParams& sp = p.s;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int jj = lane & (GS - 1), qq = lane / GS;
+  const int nit = *p.n_items;
+  int j = blockIdx.x;
+  if (j >= nit) return;  // the same for the whole block
+  const int B = gridDim.x;
+
+  // this thread's codewords (as scan2.cuh)
+  float cw[STEPS][DS];
+#pragma unroll
+  for (int s = 0; s < STEPS; ++s) {
+    const int e = (s * NW + warp) * QQ + qq;
+    const float* c = sp.codebooks_t + (int64_t(e) * m + jj) * Sh::DS4;
+#pragma unroll
+    for (int t = 0; t < DS; ++t) cw[s][t] = __ldg(c + t);
+  }
+  uint32_t lcol[MW];
+#pragma unroll
+  for (int a = 0; a < MW; ++a) lcol[a] = lm_lane_columns<GS>(lane, a);
+
+  // record of item it into slot: asynchronous copies by warp 0, completed
+  // before the barrier that ends the iteration
+  auto fetch = [&](int it, int slot) {
+    if (warp != 0 || it >= nit) return;
+    const uint8_t* src = p.records + int64_t(it) * p.rec_bytes;
+    uint8_t* dst = slots + slot * p.rec_bytes;
+    for (int c = lane; c < p.rec_bytes / 16; c += 32) lm_cp_async16(dst + 16 * c, src + 16 * c);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  auto fetch_wait = [&]() {
+    if (warp == 0) asm volatile("cp.async.wait_all;" ::: "memory");
+  };
+
+  // tables of the queries of the item in `slot` into half P
+  auto build = [&](int slot, int P) {
+    const LmHead& d = head(slot);
+    const int nq = d.nq;
+    const float* rs = resid(slot);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      if (g >= nq) break;
+      float r[DS];
+#pragma unroll
+      for (int t = 0; t < DS; ++t) r[t] = rs[g * p.dpad + jj * DS + t];
+      float* tg = tab + g * kGroupWords + 32 * P + jj;
+#pragma unroll
+      for (int s = 0; s < STEPS; ++s) {
+        const int e = (s * NW + warp) * QQ + qq;
+        float Tv = 0.f;
+#pragma unroll
+        for (int t = 0; t < DS; ++t) {
+          const float df = r[t] - cw[s][t];
+          Tv = fmaf(df, df, Tv);
+        }
+        float* row = tg + e * 64;
+#pragma unroll
+        for (int rep = 0; rep < REPS; ++rep) row[GS * ((rep + qq) & (REPS - 1))] = Tv;
+      }
+    }
+  };
+
+  uint32_t c0[MW], c1[MW];
+  auto first_codes = [&](int slot) {
+    const LmHead& d = head(slot);
+    const int nb = (d.len + 31) >> 5;
+    if (warp < nb) load_codes<MW>(sp.codes + (d.boff + warp) * 32 * m, lane, c0);
+  };
+
+  // bound pass: this lane's TQ smallest of the current item, ascending
+  uint32_t tq[TQ ? TQ : 1];
+#pragma unroll
+  for (int i = 0; i < (TQ ? TQ : 1); ++i) tq[i] = kSentinelKey;
+
+  // scan of the item in `slot` (its descriptor read into registers) from half P
+  const char* tab_bytes = reinterpret_cast<const char*>(tab);
+  auto scan = [&](int slot, auto Pc, auto GGc) {
+    constexpr int P = decltype(Pc)::value;
+    constexpr int GG = decltype(GGc)::value;
+    const LmHead& d = head(slot);
+    const int len = d.len;
+    const int64_t boff = d.boff;
+    int qv[GG];
+    uint32_t th[GG];
+#pragma unroll
+    for (int g = 0; g < GG; ++g) {
+      qv[g] = d.q[g];
+      th[g] = d.theta[g];
+    }
+    const int nb = (len + 31) >> 5;
+    const uint8_t* lcodes = sp.codes + boff * 32 * m;
+    for (int b = warp; b < nb; b += NW) {
+      if (b + NW < nb) load_codes<MW>(lcodes + int64_t(b + NW) * 32 * m, lane, c1);
+      float acc[GG][4];
+#pragma unroll
+      for (int g = 0; g < GG; ++g) acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
+      lm_lookups<MW, GG, P>(c0, tab_bytes, lcol, acc);
+      const bool valid = b * 32 + lane < len;
+      const uint32_t slot_id = uint32_t((boff + b) * 32 + lane);
+#pragma unroll
+      for (int g = 0; g < GG; ++g) {
+        const float dist = (acc[g][0] + acc[g][1]) + (acc[g][2] + acc[g][3]);
+        if constexpr (TQ > 0) {
+          const uint32_t key = valid ? __float_as_uint(dist) : kSentinelKey;
+          if (key < tq[TQ - 1]) {
+            tq[TQ - 1] = key;
+#pragma unroll
+            for (int i = TQ - 1; i > 0; --i) {
+              const uint32_t a = tq[i - 1], b = tq[i];
+              tq[i - 1] = min(a, b);
+              tq[i] = max(a, b);
+            }
+          }
+        } else {
+          lm_append(p, qv[g], valid && __float_as_uint(dist) <= th[g], dist, slot_id, lane);
+        }
+      }
+#pragma unroll
+      for (int w = 0; w < MW; ++w) c0[w] = c1[w];
+    }
+    if constexpr (TQ > 0) {
+      uint32_t* o = p.part_key + ((int64_t(qv[0]) * NW + warp) * 32 + lane) * TQ;
+#pragma unroll
+      for (int i = 0; i < TQ; ++i) {
+        o[i] = tq[i];
+        tq[i] = kSentinelKey;
+      }
+    }
+  };
+
+  fetch(j, 0);
+  fetch(j + B, 1);
+  fetch_wait();
+  __syncthreads();
+  build(0, 0);
+  first_codes(0);
+  if (tid == 0 && j + B < nit) prefetch_list(sp, head(1).list, m);
+  __syncthreads();
+
+  int t = 0;
+  auto step = [&](auto Pc) {
+    constexpr int P = decltype(Pc)::value;
+    const int cur = t % kLmSlots, nxt = (t + 1) % kLmSlots, fil = (t + 2) % kLmSlots;
+    const bool more = j + B < nit;
+    fetch(j + 2 * B, fil);
+    if (more) build(nxt, 1 - P);
+    if (TQ > 0 || head(cur).nq >= G) {
+      scan(cur, Pc, std::integral_constant<int, G>{});
+    } else {
+      if constexpr (G > 2) {
+        if (head(cur).nq == 2) scan(cur, Pc, std::integral_constant<int, 2>{});
+        else scan(cur, Pc, std::integral_constant<int, 1>{});
+      } else {
+        scan(cur, Pc, std::integral_constant<int, 1>{});
+      }
+    }
+    if (more) first_codes(nxt);
+    fetch_wait();
+    __syncthreads();  // half P may be rebuilt next; slot fil is complete
+    if (tid == 0 && j + 2 * B < nit) prefetch_list(sp, head(fil).list, m);
+    j += B;
+    ++t;
+  };
+  while (j < nit) {
+    step(std::integral_constant<int, 0>{});
+    if (j < nit) step(std::integral_constant<int, 1>{});
+  }
+}
+
+inline size_t scan_lm_smem_bytes(int G, int rec_bytes) {
+  return size_t(G) * kGroupWords * 4 + size_t(kLmSlots) * rec_bytes;
+}
+
+template <int MW, int DS, int G, int TQ>
+int launch_scan_lm(const LmParams& p, cudaStream_t s) {
+  auto kern = ivfpq_scan_lm_kernel<MW, DS, G, TQ>;
+  static_assert(G <= 3, "record head holds 3 queries");
+  const size_t smem = scan_lm_smem_bytes(G, p.rec_bytes);
+  IVFPQ_TRY(set_dynamic_smem(kern, smem));
+  kern<<<unsigned(num_sms()), kLmWarps * 32, smem, s>>>(p);
+  IVFPQ_LAUNCHED_K(kern, smem, kLmWarps * 32);
+  return IVFPQ_OK;
+}
+
+}  // namespace ivfpq
+
+#define IVFPQ_INST_SCAN_LM(MW, DS, G, TQ) \
+  template int ivfpq::launch_scan_lm<MW, DS, G, TQ>(const ivfpq::LmParams&, cudaStream_t);

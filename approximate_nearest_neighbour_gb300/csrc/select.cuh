@@ -183,9 +183,13 @@ struct WarpSelect {
   }
 
   // One candidate per lane (pass the sentinel key for "none"). Must be called
-  // by all 32 lanes together.
+  // by all 32 lanes together. A key not below the warp queue's largest can
+  // never enter it (that largest key only decreases), so it is rejected as
+  // well as one not below the lane's own largest: on a stream of good
+  // candidates (a query's nearest list) this keeps the thread queues from
+  // filling with keys the next merge would discard.
   __device__ __forceinline__ void add(uint32_t key, uint32_t idx) {
-    bool pass = key < tk[T - 1];
+    bool pass = key < min(tk[T - 1], wmax);
     if (__any_sync(kFullMask, pass)) {
       if (pass) {
         tk[T - 1] = key;

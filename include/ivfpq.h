@@ -192,15 +192,38 @@ int ivfpq_stage_times(const ivfpq_index* index, float* ms, int* nsearches);
  */
 int ivfpq_set_precomputed(ivfpq_index* index, int mode);
 
+/*
+ * ivfpq_set_scan_mode -- how later searches of the index organise the list
+ * scan; results are the same either way (up to the order of equal distances).
+ * Source: "Billion-scale similarity search with GPUs", section 5: queries x
+ * lists are independent work, taken there query by query.
+ *  mode   -1 automatic (default): by list where the shapes allow it (fp32
+ *            tables, direct tables, (m, d/m) in {(32,3), (32,4), (16,8),
+ *            (16,4), (8,12), (8,8)}, nprobe >= 2) and the batch probes every
+ *            list twice or more on average, else by query;
+ *          0 by query: one thread block per (query, chunk of its lists);
+ *          1 by list where the shapes allow it: the queries that probe a
+ *            list are scanned together, `group` of them per table set, each
+ *            keeping the codes within the k-th distance of its nearest list
+ *            (which is scanned first, by query); a query with more such codes
+ *            than its buffer holds is scanned again by query
+ *  group  queries per table set of the by-list scan: 2 or 3 (0 keeps the
+ *         current value; default 3)
+ * Errors: INVALID_ARG.
+ */
+int ivfpq_set_scan_mode(ivfpq_index* index, int mode, int group);
+
 /* ivfpq_uses_precomputed -- 1 if searches of the index currently use the
  * precomputed-term tables, else 0. */
 int ivfpq_uses_precomputed(const ivfpq_index* index);
 
 /* ivfpq_last_scan_kernel -- name of the list-scan kernel family that the
- * most recent search of this index launched ("ivfpq_scan2_kernel": codebook
- * in registers, double-buffered fp32 tables, used for fp32 tables with (m,
- * d/m) in {(32,3), (32,4), (16,8), (16,4), (8,12), (8,8)}; "ivfpq_scan_kernel": the general
- * kernel), or NULL before the first search; a measurement aid. */
+ * most recent search of this index launched ("ivfpq_scan_lm_kernel": the
+ * by-list scan of ivfpq_set_scan_mode; "ivfpq_scan2_kernel": by query,
+ * codebook in registers, double-buffered fp32 tables, used for fp32 tables
+ * with (m, d/m) in {(32,3), (32,4), (16,8), (16,4), (8,12), (8,8)};
+ * "ivfpq_scan_kernel": the general kernel), or NULL before the first search;
+ * a measurement aid. */
 const char* ivfpq_last_scan_kernel(const ivfpq_index* index);
 
 /* ivfpq_kernel_launches -- number of CUDA kernels this library has launched

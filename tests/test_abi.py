@@ -90,6 +90,7 @@ def test_host_side_argument_errors_of_the_other_entries(lib):
         lambda: lib.ivfpq_search_preassigned(None, vp, 1, 1, vp, 1, vp, vp, None),
         lambda: lib.ivfpq_search_probes(None, vp, 1, 1, vp, vp, None),
         lambda: lib.ivfpq_set_precomputed(None, 0),
+        lambda: lib.ivfpq_set_scan_mode(None, 1, 2),
         # merge: k beyond the limit, no shards, null inputs
         lambda: lib.knn_merge(vp, vp, 4, 2, 10, 2049, vp, vp, None),
         lambda: lib.knn_merge(vp, vp, 4, 0, 10, 5, vp, vp, None),

@@ -110,8 +110,59 @@ def test_code_widths_and_ragged_lists(B, m, dsub):
     codes, list_ids, ids = S.shuffled(data, w.number)
     ix = make_index(B, data.cent, data.cb, codes, list_ids, ids)
     lists = oracle.to_lists(codes, list_ids, ids, w.nlist)
-    for k in (1, 33, 250):
-        search_and_check(B, ix, data.cent, data.cb, lists, q, 7, k, context=f"m={m} k={k}")
+    for mode in (0, -1):  # by query, then automatic (by list for its shapes)
+        B.ivfpq_set_scan_mode(ix, mode)
+        for k in (1, 33, 250):
+            search_and_check(B, ix, data.cent, data.cb, lists, q, 7, k,
+                             context=f"m={m} k={k} mode={mode}")
+
+
+LM_SHAPES = [(32, 3), (32, 4), (16, 8), (16, 4), (8, 12), (8, 8)]
+
+
+@pytest.mark.parametrize("group", [2, 3])
+@pytest.mark.parametrize("m,dsub", LM_SHAPES)
+def test_list_major_scan_follows_the_oracle(B, m, dsub, group):
+    """The by-list scan (queries of a list scanned together, a bound from each
+    query's nearest list, candidate buffers) on ragged and empty lists, many
+    queries per list, k from 1 to 2048."""
+    w = S.IVFPQWorkload("t", 200 + m + dsub, 40_000, m * dsub, 61, m, 0.15, True, 300, (9,),
+                        (33,), ("fp32",))
+    data = S.compressed_index(w)
+    q = S.queries(w.number, data.cent, data.weights, w.sigma, w.nq)
+    codes, list_ids, ids = S.shuffled(data, w.number)
+    ix = make_index(B, data.cent, data.cb, codes, list_ids, ids)
+    B.ivfpq_set_scan_mode(ix, 1, group)
+    lists = oracle.to_lists(codes, list_ids, ids, w.nlist)
+    for k in (1, 100, 1000, 2048):
+        search_and_check(B, ix, data.cent, data.cb, lists, q, 9, k, rows=np.arange(0, 300, 7),
+                         context=f"list-major m={m} G={group} k={k}")
+        assert B.last_scan_kernel(ix) == "ivfpq_scan_lm_kernel"
+
+
+@pytest.mark.parametrize("group", [2, 3])
+def test_list_major_candidate_overflow_is_rescanned(B, group):
+    """Every query's nearest list holds fewer than k codes, so its bound is
+    +inf and all codes of the other probed lists are candidates, more than
+    the buffer holds: those queries are scanned again by query."""
+    rng = np.random.default_rng(71 + group)
+    nlist, m, dsub = 6, 32, 3
+    d = m * dsub
+    cent = rng.standard_normal((nlist, d)).astype(np.float32) * 3
+    cb = (0.3 * rng.standard_normal((m, 256, dsub))).astype(np.float32)
+    sizes = [5, 900, 900, 900, 900, 900]
+    list_ids = np.repeat(np.arange(nlist, dtype=np.int32), sizes)
+    n = list_ids.shape[0]
+    codes = rng.integers(0, 256, (n, m)).astype(np.uint8)
+    ids = np.arange(n, dtype=np.int64) * 5 + 2
+    ix = make_index(B, cent, cb, codes, list_ids, ids)
+    B.ivfpq_set_scan_mode(ix, 1, group)
+    q = (cent[0] + 0.05 * rng.standard_normal((40, d))).astype(np.float32)
+    lists = oracle.to_lists(codes, list_ids, ids, nlist)
+    B.ivfpq_repaired_queries(ix)
+    search_and_check(B, ix, cent, cb, lists, q, 5, 10, context="overflow")
+    assert B.ivfpq_repaired_queries(ix) >= 40  # every query overflowed
+    assert B.last_scan_kernel(ix) == "ivfpq_scan_lm_kernel"
 
 
 def test_empty_lists_large_k_and_padding(B):
