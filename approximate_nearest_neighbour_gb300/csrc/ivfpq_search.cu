@@ -579,7 +579,6 @@ int scan_stage_lm(const ivfpq_index* ix, const float* queries, int64_t nq, int n
                   cudaStream_t s) {
   auto* mix = const_cast<ivfpq_index*>(ix);
   Workspace ws(s);
-  record(ix, 2, s);
   const ScanParams base = scan_params(ix, queries, nq, nprobe, probes, k);
   // 1. bound pass: per query, 512 lane queues of tq over its nearest list
   //    (512 * tq >= 2k), and the k-th smallest of their entries
@@ -618,6 +617,9 @@ int scan_stage_lm(const ivfpq_index* ix, const float* queries, int64_t nq, int n
   IVFPQ_TRY(ws.alloc(&lp.cid, size_t(nq) * cap));
   IVFPQ_TRY(ws.alloc(&lp.ccount, size_t(nq)));
   IVFPQ_CUDA(cudaMemsetAsync(lp.ccount, 0, size_t(nq) * sizeof(int), s));
+  // stage timing: the bound pass and the planning count as stage 1, the
+  // filter kernel alone as stage 2
+  record(ix, 2, s);
   if (G >= 3) IVFPQ_TRY((try_scan_lm<3, 0>(lp, s, &launched)));
   else IVFPQ_TRY((try_scan_lm<2, 0>(lp, s, &launched)));
   IVFPQ_REQUIRE(launched, "scan: no list-major kernel for m=%d d/m=%d", ix->m, ix->dsub);

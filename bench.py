@@ -41,7 +41,8 @@ from approximate_nearest_neighbour_gb300 import synthetic as S  # noqa: E402
 FALLBACK_HBM_GBS = 6800.0
 # ncu summary of the scan kernel on the large workload, per kernel family
 PROFILE_FILE = os.path.join(ROOT, "profiles", "{kernel}_large.md")
-SCAN_SOURCES = ["scan2.cuh", "scan.cuh", "select.cuh", "layout.cuh", "common.cuh"]
+SCAN_SOURCES = ["scan_lm.cuh", "scan2.cuh", "scan.cuh", "select.cuh", "layout.cuh", "common.cuh"]
+LOOKUPS_PER_SM_CLOCK = 32  # one 4-byte shared-memory word per bank and clock, 32 banks
 
 
 def parse():
@@ -59,6 +60,8 @@ def parse():
                    help="large (default, the headline), mid, billion, flat (exact k-NN) "
                         "or kselect (stand-alone k-selection)")
     p.add_argument("--k", type=int, default=None, help="k override")
+    p.add_argument("--scan-mode", type=int, default=-1, choices=[-1, 0, 1],
+                   help="list scan organisation: -1 automatic, 0 by query, 1 by list")
     return p.parse_args()
 
 
@@ -76,6 +79,16 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def sm_max_mhz():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        if pk.get("sm_max_mhz"):
+            return float(pk["sm_max_mhz"])
+    return 2070.0
 
 
 def peaks():
@@ -279,7 +292,8 @@ def config_dict(args, n, nlist):
     scaled = args.n is not None or args.nlist is not None
     return {"workload": w.name if not scaled else f"{w.name}(N={n},nlist={nlist})", "n": n,
             "d": w.d, "nlist": nlist, "m": w.m, "nq_per_gpu": args.nq or w.nq, "nprobe": NPROBE, "k": K,
-            "lut": args.lut, "parallelism": f"replicas x{args.gpus}",
+            "lut": args.lut, "scan_mode": {-1: "automatic", 0: "by query", 1: "by list"}[
+                args.scan_mode], "parallelism": f"replicas x{args.gpus}",
             "index": "centroids = mixture centres; PQ codebooks trained by 10 Lloyd iterations "
                      "on the residuals of 262,144 rows; every vector encoded by nearest centroid "
                      "and nearest codeword on the GPU",
@@ -313,6 +327,7 @@ def run_ours(args):
     q = S.queries(w.number, wi.cent, wi.weights, w.sigma, args.nq or w.nq, salt=rank)
     nq = q.shape[0]
     B.ivfpq_set_lut_type(ix, args.lut)
+    B.ivfpq_set_scan_mode(ix, args.scan_mode)
     qd = torch.from_numpy(q).to(dev)
     out_d = torch.empty((nq, K), dtype=torch.float32, device=dev)
     out_i = torch.empty((nq, K), dtype=torch.int64, device=dev)
@@ -390,6 +405,11 @@ def run_ours(args):
         scan_ms = sums[2] / max(count, 1)
         achieved = scan_bytes / (scan_ms / 1e3) / 1e9
         traffic = profiled_traffic(scan_kernel)
+        # the look-up bound: one shared-memory word per code byte
+        nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+        sm_mhz = sm_max_mhz()
+        lookup_peak = nsm * LOOKUPS_PER_SM_CLOCK * sm_mhz * 1e6
+        lookups_per_s = scan_bytes / (scan_ms / 1e3)
         if traffic is not None and (args.n is not None or args.nlist is not None
                                     or args.workload != "large"):
             traffic = None
@@ -409,8 +429,13 @@ def run_ours(args):
                          "peak_source": f"{peak_kind} hbm_gbs (copy)",
                          "traffic": traffic, "algorithmic_bytes_per_launch": scan_bytes,
                          "launch_ms": scan_ms},
-            "stage_ms": {"coarse": sums[0] / max(count, 1), "scan": scan_ms,
-                         "merge": sums[3] / max(count, 1)},
+            "lookup_roofline": {"bound": "shared-memory look-ups", "kernel": scan_kernel,
+                                "achieved": lookups_per_s / 1e12, "unit": "Tlookups/s",
+                                "peak": lookup_peak / 1e12, "frac": lookups_per_s / lookup_peak,
+                                "peak_source": f"{nsm} SMs x {LOOKUPS_PER_SM_CLOCK} banks x "
+                                               f"{sm_mhz:.0f} MHz"},
+            "stage_ms": {"coarse": sums[0] / max(count, 1), "plan": sums[1] / max(count, 1),
+                         "scan": scan_ms, "merge": sums[3] / max(count, 1)},
             "scanned_codes_per_s": scanned_codes / (scan_ms / 1e3) * world,
             "e2e": {"value": total_q / e2e_elapsed, "unit": "queries/s",
                     "h2d_bytes_per_step": int(q.nbytes),

@@ -165,10 +165,12 @@ int ivfpq_search_preassigned(const ivfpq_index* index, const float* queries, int
  * `stream` around its stages (up to 4096 searches are kept).
  * ivfpq_stage_times waits for the recorded events and writes, summed over
  * the recorded searches, the milliseconds of [0] coarse quantizer (distances
- * + top-nprobe), [1] grouping / planning, [2] lookup tables + list scan +
- * per-chunk selection, [3] cross-list merge into ms[0..3], and the number of
- * recorded searches into *nsearches (may be NULL). Stages that did not run
- * contribute 0.
+ * + top-nprobe), [1] planning (by-list scan: the bound pass over each
+ * query's nearest list, the (list, query) items and their records),
+ * [2] the list-scan kernel (lookup tables + list scan + per-chunk selection
+ * or candidate filter), [3] merge / final selection and rescans into
+ * ms[0..3], and the number of recorded searches into *nsearches (may be
+ * NULL). Stages that did not run contribute 0.
  */
 int ivfpq_set_profiling(ivfpq_index* index, int enable);
 int ivfpq_stage_times(const ivfpq_index* index, float* ms, int* nsearches);
