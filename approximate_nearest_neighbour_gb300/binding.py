@@ -299,7 +299,7 @@ def ivfpq_set_precomputed(index, mode):
 
 def ivfpq_set_scan_mode(index, mode, group=0):
     """-1 automatic, 0 by query, 1 by list (where its shapes apply); group =
-    queries per table set of the by-list scan (2 or 3; 0 keeps it)."""
+    table sets per by-list item (2 or 3, -1 automatic, 0 keeps it)."""
     _check("ivfpq_set_scan_mode", lib().ivfpq_set_scan_mode(index.handle, int(mode), int(group)))
 
 

@@ -138,9 +138,9 @@ struct ivfpq_index {
   float* term1 = nullptr;
   int precomputed = -1;
   // list scan organisation: -1 automatic, 0 by query, 1 by list (list-major,
-  // where its shapes apply); the queries per list sharing one table set
+  // where its shapes apply); table sets per by-list item (0 automatic)
   int scan_mode = -1;
-  int lm_group = 3;
+  int lm_group = 0;
   // tensor-core operands of the centroids (null when that path is unavailable)
   float* cent_hi = nullptr;     // [nlist, tc_dpad(d)]
   float* cent_lo = nullptr;

@@ -72,12 +72,21 @@ int try_scan2_kw(const ScanParams& p, int64_t nq, cudaStream_t s, int* launched)
   return IVFPQ_OK;
 }
 
-#define IVFPQ_EXTERN_SCAN_LM(MW, DS)                                                     \
-  extern template int launch_scan_lm<MW, DS, 2, 0>(const LmParams&, cudaStream_t);     \
-  extern template int launch_scan_lm<MW, DS, 3, 0>(const LmParams&, cudaStream_t);     \
-  extern template int launch_scan_lm<MW, DS, 1, 2>(const LmParams&, cudaStream_t);     \
-  extern template int launch_scan_lm<MW, DS, 1, 4>(const LmParams&, cudaStream_t);     \
-  extern template int launch_scan_lm<MW, DS, 1, 8>(const LmParams&, cudaStream_t);
+#define IVFPQ_EXTERN_SCAN_LM_LT(MW, DS, LT)                                           \
+  extern template int launch_scan_lm<MW, DS, 1, 2, LT>(const LmParams&, cudaStream_t); \
+  extern template int launch_scan_lm<MW, DS, 1, 4, LT>(const LmParams&, cudaStream_t); \
+  extern template int launch_scan_lm<MW, DS, 1, 8, LT>(const LmParams&, cudaStream_t);
+#define IVFPQ_EXTERN_SCAN_LM(MW, DS)                                                         \
+  extern template int launch_scan_lm<MW, DS, 2, 0, IVFPQ_LUT_FP32>(const LmParams&,          \
+                                                                   cudaStream_t);            \
+  extern template int launch_scan_lm<MW, DS, 3, 0, IVFPQ_LUT_FP32>(const LmParams&,          \
+                                                                   cudaStream_t);            \
+  extern template int launch_scan_lm<MW, DS, 4, 0, IVFPQ_LUT_FP16>(const LmParams&,          \
+                                                                   cudaStream_t);            \
+  extern template int launch_scan_lm<MW, DS, 6, 0, IVFPQ_LUT_FP16>(const LmParams&,          \
+                                                                   cudaStream_t);            \
+  IVFPQ_EXTERN_SCAN_LM_LT(MW, DS, IVFPQ_LUT_FP32)                                            \
+  IVFPQ_EXTERN_SCAN_LM_LT(MW, DS, IVFPQ_LUT_FP16)
 IVFPQ_EXTERN_SCAN_LM(8, 3)
 IVFPQ_EXTERN_SCAN_LM(8, 4)
 IVFPQ_EXTERN_SCAN_LM(4, 8)
@@ -87,19 +96,29 @@ IVFPQ_EXTERN_SCAN_LM(2, 8)
 
 // The list-major kernel (scan_lm.cuh): the filter pass with G queries per
 // table set (TQ = 0) or the bound pass with TQ-entry lane queues (G = 1).
-template <int G, int KW>
+template <int G, int TQ, int LT>
 int try_scan_lm(const LmParams& p, cudaStream_t s, int* launched) {
   *launched = 1;
   switch (p.s.m * 100 + p.s.dsub) {
-    case 3203: return launch_scan_lm<8, 3, G, KW>(p, s);
-    case 3204: return launch_scan_lm<8, 4, G, KW>(p, s);
-    case 1608: return launch_scan_lm<4, 8, G, KW>(p, s);
-    case 1604: return launch_scan_lm<4, 4, G, KW>(p, s);
-    case 812: return launch_scan_lm<2, 12, G, KW>(p, s);
-    case 808: return launch_scan_lm<2, 8, G, KW>(p, s);
+    case 3203: return launch_scan_lm<8, 3, G, TQ, LT>(p, s);
+    case 3204: return launch_scan_lm<8, 4, G, TQ, LT>(p, s);
+    case 1608: return launch_scan_lm<4, 8, G, TQ, LT>(p, s);
+    case 1604: return launch_scan_lm<4, 4, G, TQ, LT>(p, s);
+    case 812: return launch_scan_lm<2, 12, G, TQ, LT>(p, s);
+    case 808: return launch_scan_lm<2, 8, G, TQ, LT>(p, s);
   }
   *launched = 0;
   return IVFPQ_OK;
+}
+
+// The bound pass with TQ-entry lane queues, tables of type LT.
+template <int LT>
+int launch_bound_pass(const LmParams& p, int tq, cudaStream_t s, int* launched) {
+  switch (tq) {
+    case 2: return try_scan_lm<1, 2, LT>(p, s, launched);
+    case 4: return try_scan_lm<1, 4, LT>(p, s, launched);
+    default: return try_scan_lm<1, 8, LT>(p, s, launched);
+  }
 }
 
 bool scan2_shape(const ScanParams& p) {
@@ -505,6 +524,7 @@ bool use_list_major(const ivfpq_index* ix, int64_t nq, int nprobe) {
   p.d = ix->d;
   p.k = 1;
   p.lut_type = ix->lut_type;
+  if (ix->lut_type == IVFPQ_LUT_FP16) p.lut_type = IVFPQ_LUT_FP32;  // by list: fp32 or binary16
   if (!scan2_shape(p)) return false;
   if (ix->scan_mode == 1) return true;
   return double(nq) * nprobe >= 2.0 * ix->nlist;
@@ -592,11 +612,9 @@ int scan_stage_lm(const ivfpq_index* ix, const float* queries, int64_t nq, int n
   IVFPQ_TRY(ws.alloc(&bp.part_key, npart));
   IVFPQ_CUDA(cudaMemsetAsync(bp.part_key, 0xff, npart * sizeof(uint32_t), s));
   int launched = 0;
-  switch (tq) {
-    case 2: IVFPQ_TRY((try_scan_lm<1, 2>(bp, s, &launched))); break;
-    case 4: IVFPQ_TRY((try_scan_lm<1, 4>(bp, s, &launched))); break;
-    default: IVFPQ_TRY((try_scan_lm<1, 8>(bp, s, &launched))); break;
-  }
+  const bool half = ix->lut_type == IVFPQ_LUT_FP16;
+  if (half) IVFPQ_TRY(launch_bound_pass<IVFPQ_LUT_FP16>(bp, tq, s, &launched));
+  else IVFPQ_TRY(launch_bound_pass<IVFPQ_LUT_FP32>(bp, tq, s, &launched));
   IVFPQ_REQUIRE(launched, "scan: no list-major kernel for m=%d d/m=%d", ix->m, ix->dsub);
   uint32_t* theta = nullptr;
   IVFPQ_TRY(ws.alloc(&theta, size_t(nq)));
@@ -605,14 +623,19 @@ int scan_stage_lm(const ivfpq_index* ix, const float* queries, int64_t nq, int n
   // 2. filter pass over all the probed lists
   LmParams lp;
   lp.s = base;
-  const int G = ix->lm_group;
+  // table sets per item (fp32: one query each, binary16: two); automatic:
+  // the fastest measured (search ms, 10,000 queries, 2 / 3 sets: fp32 large
+  // 13.02 / 12.29; binary16 billion 21.40 / 20.06, large 10.73 / 10.66, mid
+  // 7.72 / 8.45)
+  const int sets = ix->lm_group ? ix->lm_group : (half && ix->m == 16) ? 2 : 3;
+  const int G = sets * (half ? 2 : 1);
   IVFPQ_TRY(plan_items(probes, nq, nprobe, 0, nprobe, G, ix->nlist, ws, s, lp));
   const int cap = std::max(1024, 2 * k);
   lp.theta_key = theta;
   lp.theta_stride = 1;
   lp.ids = ix->ids;
   lp.cap = cap;
-  IVFPQ_TRY(make_records(lp, G >= 3 ? 3 : 2, false, ws, s));
+  IVFPQ_TRY(make_records(lp, G, false, ws, s));
   IVFPQ_TRY(ws.alloc(&lp.ckey, size_t(nq) * cap));
   IVFPQ_TRY(ws.alloc(&lp.cid, size_t(nq) * cap));
   IVFPQ_TRY(ws.alloc(&lp.ccount, size_t(nq)));
@@ -620,8 +643,13 @@ int scan_stage_lm(const ivfpq_index* ix, const float* queries, int64_t nq, int n
   // stage timing: the bound pass and the planning count as stage 1, the
   // filter kernel alone as stage 2
   record(ix, 2, s);
-  if (G >= 3) IVFPQ_TRY((try_scan_lm<3, 0>(lp, s, &launched)));
-  else IVFPQ_TRY((try_scan_lm<2, 0>(lp, s, &launched)));
+  if (half) {
+    if (G >= 6) IVFPQ_TRY((try_scan_lm<6, 0, IVFPQ_LUT_FP16>(lp, s, &launched)));
+    else IVFPQ_TRY((try_scan_lm<4, 0, IVFPQ_LUT_FP16>(lp, s, &launched)));
+  } else {
+    if (G >= 3) IVFPQ_TRY((try_scan_lm<3, 0, IVFPQ_LUT_FP32>(lp, s, &launched)));
+    else IVFPQ_TRY((try_scan_lm<2, 0, IVFPQ_LUT_FP32>(lp, s, &launched)));
+  }
   IVFPQ_REQUIRE(launched, "scan: no list-major kernel for m=%d d/m=%d", ix->m, ix->dsub);
   mix->last_scan_kernel.store("ivfpq_scan_lm_kernel");
   record(ix, 3, s);
@@ -793,10 +821,11 @@ extern "C" int ivfpq_set_scan_mode(ivfpq_index* ix, int mode, int group) {
   clear_error();
   IVFPQ_REQUIRE(ix, "ivfpq_set_scan_mode: null index");
   IVFPQ_REQUIRE(mode >= -1 && mode <= 1, "ivfpq_set_scan_mode: mode=%d outside [-1, 1]", mode);
-  IVFPQ_REQUIRE(group == 0 || group == 2 || group == 3,
-                "ivfpq_set_scan_mode: group=%d (0 keeps the current, else 2 or 3)", group);
+  IVFPQ_REQUIRE(group >= -1 && group <= 3 && group != 1,
+                "ivfpq_set_scan_mode: group=%d (0 keeps the current, -1 automatic, else 2 or 3)",
+                group);
   ix->scan_mode = mode;
-  if (group) ix->lm_group = group;
+  if (group) ix->lm_group = group < 0 ? 0 : group;
   return IVFPQ_OK;
 }
 

@@ -42,6 +42,7 @@ namespace ivfpq {
 
 constexpr int kLmWarps = 16;
 constexpr int kLmSlots = 3;  // item descriptors in flight: scanned, built, fetched
+constexpr int kLmMaxG = 8;   // queries per item at most
 
 struct LmParams {
   ScanParams s;                // tables, lists, codes, shapes (nprobe unused)
@@ -73,10 +74,10 @@ struct LmParams {
 struct LmHead {
   int list, len, nq, pad;
   int64_t boff;
-  int q[3];
-  uint32_t theta[3];
+  int q[kLmMaxG];
+  uint32_t theta[kLmMaxG];
 };
-constexpr int kLmHead = 64;
+constexpr int kLmHead = 128;
 static_assert(sizeof(LmHead) <= kLmHead, "record head");
 
 inline int lm_record_bytes(int G, int d) { return kLmHead + G * ((d + 3) & ~3) * 4; }
@@ -125,6 +126,28 @@ __device__ __forceinline__ void lm_lookups(const uint32_t (&w)[MW], const char* 
   }
 }
 
+// binary16 tables: word (row, column) of table set g holds the entries of
+// queries 2g (low half) and 2g + 1 (high half); each is added to its fp32
+// sum (mixed-precision add: exact conversion, one rounding). NC sums per
+// query (4, or 2 with three table sets, where 4 would spill registers).
+template <int MW, int NS, int NC, int P, int S = 0>
+__device__ __forceinline__ void lm_lookups_h(const uint32_t (&w)[MW], const char* tab,
+                                             const uint32_t (&lcol)[MW], float (&acc)[2 * NS][4]) {
+  if constexpr (S < 4 * MW) {
+    constexpr int SEL = 0xCC00 | ((S & 3) << 4) | (4 + (S & 3));
+    const uint32_t off = lm_prmt<SEL>(w[S >> 2], lcol[S >> 2]);
+#pragma unroll
+    for (int g = 0; g < NS; ++g) {
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(tab + off + g * 65536 + 128 * P);
+      asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+          "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+          : "+f"(acc[2 * g][S % NC]), "+f"(acc[2 * g + 1][S % NC])
+          : "r"(v));
+    }
+    lm_lookups_h<MW, NS, NC, P, S + 1>(w, tab, lcol, acc);
+  }
+}
+
 // Appends (dist, id of slot) to query q's candidates where `pass` holds.
 // All 32 lanes call it together.
 __device__ __forceinline__ void lm_append(const LmParams& p, int q, bool pass, float dist,
@@ -145,9 +168,13 @@ __device__ __forceinline__ void lm_append(const LmParams& p, int q, bool pass, f
   }
 }
 
-template <int MW, int DS, int G, int TQ>
+template <int MW, int DS, int G, int TQ, int LT>
 __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const LmParams p) {
   static_assert(TQ == 0 || G == 1, "the bound pass takes one query per item");
+  static_assert(LT == IVFPQ_LUT_FP32 || LT == IVFPQ_LUT_FP16, "fp32 or binary16 tables");
+  static_assert(G <= kLmMaxG, "record head");
+  constexpr bool H = LT == IVFPQ_LUT_FP16;
+  constexpr int NS = H ? (G + 1) / 2 : G;  // table sets
   using Sh = Scan2Shape<MW, DS>;
   constexpr int NW = kLmWarps;
   constexpr int m = Sh::M;
@@ -157,8 +184,8 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
   constexpr int REPS = 32 / GS;
   static_assert(kScan2Warps == NW, "codeword ownership as in scan2.cuh");
   extern __shared__ __align__(16) uint32_t lm_smem[];
-  float* tab = reinterpret_cast<float*>(lm_smem);  // G x [256][64] fp32
-  uint8_t* slots = reinterpret_cast<uint8_t*>(lm_smem + G * kGroupWords);
+  float* tab = reinterpret_cast<float*>(lm_smem);  // NS x [256][64] 4-byte words
+  uint8_t* slots = reinterpret_cast<uint8_t*>(lm_smem + NS * kGroupWords);
   auto head = [&](int slot) -> const LmHead& {
     return *reinterpret_cast<const LmHead*>(slots + slot * p.rec_bytes);
   };
@@ -200,29 +227,46 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
   };
 
   // tables of the queries of the item in `slot` into half P
+  auto entry = [&](const float (&r)[DS], int s) {
+    float Tv = 0.f;
+#pragma unroll
+    for (int t = 0; t < DS; ++t) {
+      const float df = r[t] - cw[s][t];
+      Tv = fmaf(df, df, Tv);
+    }
+    return Tv;
+  };
   auto build = [&](int slot, int P) {
     const LmHead& d = head(slot);
     const int nq = d.nq;
     const float* rs = resid(slot);
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      if (g >= nq) break;
-      float r[DS];
+    for (int g = 0; g < NS; ++g) {
+      if ((H ? 2 * g : g) >= nq) break;
+      float r[DS], r2[DS];
 #pragma unroll
-      for (int t = 0; t < DS; ++t) r[t] = rs[g * p.dpad + jj * DS + t];
-      float* tg = tab + g * kGroupWords + 32 * P + jj;
+      for (int t = 0; t < DS; ++t) r[t] = rs[(H ? 2 * g : g) * p.dpad + jj * DS + t];
+      const bool two = H && 2 * g + 1 < nq;
+      if constexpr (H) {
+#pragma unroll
+        for (int t = 0; t < DS; ++t) r2[t] = two ? rs[(2 * g + 1) * p.dpad + jj * DS + t] : 0.f;
+      }
+      uint32_t* tg = reinterpret_cast<uint32_t*>(tab) + g * kGroupWords + 32 * P + jj;
 #pragma unroll
       for (int s = 0; s < STEPS; ++s) {
         const int e = (s * NW + warp) * QQ + qq;
-        float Tv = 0.f;
-#pragma unroll
-        for (int t = 0; t < DS; ++t) {
-          const float df = r[t] - cw[s][t];
-          Tv = fmaf(df, df, Tv);
+        uint32_t word;
+        if constexpr (H) {
+          const float T0 = entry(r, s);
+          const float T1 = two ? entry(r2, s) : 0.f;
+          word = uint32_t(__half_as_ushort(__float2half_rn(T0))) |
+                 (uint32_t(__half_as_ushort(__float2half_rn(T1))) << 16);
+        } else {
+          word = __float_as_uint(entry(r, s));
         }
-        float* row = tg + e * 64;
+        uint32_t* row = tg + e * 64;
 #pragma unroll
-        for (int rep = 0; rep < REPS; ++rep) row[GS * ((rep + qq) & (REPS - 1))] = Tv;
+        for (int rep = 0; rep < REPS; ++rep) row[GS * ((rep + qq) & (REPS - 1))] = word;
       }
     }
   };
@@ -247,21 +291,24 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
     const LmHead& d = head(slot);
     const int len = d.len;
     const int64_t boff = d.boff;
+    const int nqi = d.nq;
     int qv[GG];
     uint32_t th[GG];
 #pragma unroll
     for (int g = 0; g < GG; ++g) {
-      qv[g] = d.q[g];
-      th[g] = d.theta[g];
+      qv[g] = g < nqi ? d.q[g] : 0;
+      th[g] = g < nqi ? d.theta[g] : 0u;
     }
     const int nb = (len + 31) >> 5;
     const uint8_t* lcodes = sp.codes + boff * 32 * m;
     for (int b = warp; b < nb; b += NW) {
       if (b + NW < nb) load_codes<MW>(lcodes + int64_t(b + NW) * 32 * m, lane, c1);
-      float acc[GG][4];
+      constexpr int NA = H ? 2 * ((GG + 1) / 2) : GG;
+      float acc[NA][4];
 #pragma unroll
-      for (int g = 0; g < GG; ++g) acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
-      lm_lookups<MW, GG, P>(c0, tab_bytes, lcol, acc);
+      for (int g = 0; g < NA; ++g) acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
+      if constexpr (H) lm_lookups_h<MW, (GG + 1) / 2, (GG > 4 ? 2 : 4), P>(c0, tab_bytes, lcol, acc);
+      else lm_lookups<MW, GG, P>(c0, tab_bytes, lcol, acc);
       const bool valid = b * 32 + lane < len;
       const uint32_t slot_id = uint32_t((boff + b) * 32 + lane);
 #pragma unroll
@@ -278,7 +325,7 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
               tq[i] = max(a, b);
             }
           }
-        } else {
+        } else if (g < nqi) {
           lm_append(p, qv[g], valid && __float_as_uint(dist) <= th[g], dist, slot_id, lane);
         }
       }
@@ -311,11 +358,24 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
     const bool more = j + B < nit;
     fetch(j + 2 * B, fil);
     if (more) build(nxt, 1 - P);
-    if (TQ > 0 || head(cur).nq >= G) {
+    const int nqc = head(cur).nq;
+    if (TQ > 0 || nqc >= G) {
       scan(cur, Pc, std::integral_constant<int, G>{});
+    } else if constexpr (H) {
+      // binary16: whole table sets (pairs of queries)
+      if constexpr (G > 4) {
+        if (nqc > 4) scan(cur, Pc, std::integral_constant<int, 6>{});
+        else if (nqc > 2) scan(cur, Pc, std::integral_constant<int, 4>{});
+        else scan(cur, Pc, std::integral_constant<int, 2>{});
+      } else if constexpr (G > 2) {
+        if (nqc > 2) scan(cur, Pc, std::integral_constant<int, 4>{});
+        else scan(cur, Pc, std::integral_constant<int, 2>{});
+      } else {
+        scan(cur, Pc, std::integral_constant<int, 2>{});
+      }
     } else {
       if constexpr (G > 2) {
-        if (head(cur).nq == 2) scan(cur, Pc, std::integral_constant<int, 2>{});
+        if (nqc == 2) scan(cur, Pc, std::integral_constant<int, 2>{});
         else scan(cur, Pc, std::integral_constant<int, 1>{});
       } else {
         scan(cur, Pc, std::integral_constant<int, 1>{});
@@ -334,15 +394,15 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
   }
 }
 
-inline size_t scan_lm_smem_bytes(int G, int rec_bytes) {
-  return size_t(G) * kGroupWords * 4 + size_t(kLmSlots) * rec_bytes;
+inline size_t scan_lm_smem_bytes(int sets, int rec_bytes) {
+  return size_t(sets) * kGroupWords * 4 + size_t(kLmSlots) * rec_bytes;
 }
 
-template <int MW, int DS, int G, int TQ>
+template <int MW, int DS, int G, int TQ, int LT>
 int launch_scan_lm(const LmParams& p, cudaStream_t s) {
-  auto kern = ivfpq_scan_lm_kernel<MW, DS, G, TQ>;
-  static_assert(G <= 3, "record head holds 3 queries");
-  const size_t smem = scan_lm_smem_bytes(G, p.rec_bytes);
+  auto kern = ivfpq_scan_lm_kernel<MW, DS, G, TQ, LT>;
+  const int sets = LT == IVFPQ_LUT_FP16 ? (G + 1) / 2 : G;
+  const size_t smem = scan_lm_smem_bytes(sets, p.rec_bytes);
   IVFPQ_TRY(set_dynamic_smem(kern, smem));
   kern<<<unsigned(num_sms()), kLmWarps * 32, smem, s>>>(p);
   IVFPQ_LAUNCHED_K(kern, smem, kLmWarps * 32);
@@ -351,5 +411,5 @@ int launch_scan_lm(const LmParams& p, cudaStream_t s) {
 
 }  // namespace ivfpq
 
-#define IVFPQ_INST_SCAN_LM(MW, DS, G, TQ) \
-  template int ivfpq::launch_scan_lm<MW, DS, G, TQ>(const ivfpq::LmParams&, cudaStream_t);
+#define IVFPQ_INST_SCAN_LM(MW, DS, G, TQ, LT) \
+  template int ivfpq::launch_scan_lm<MW, DS, G, TQ, LT>(const ivfpq::LmParams&, cudaStream_t);

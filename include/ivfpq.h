@@ -200,17 +200,18 @@ int ivfpq_set_precomputed(ivfpq_index* index, int mode);
  * Source: "Billion-scale similarity search with GPUs", section 5: queries x
  * lists are independent work, taken there query by query.
  *  mode   -1 automatic (default): by list where the shapes allow it (fp32
- *            tables, direct tables, (m, d/m) in {(32,3), (32,4), (16,8),
- *            (16,4), (8,12), (8,8)}, nprobe >= 2) and the batch probes every
- *            list twice or more on average, else by query;
+ *            or binary16 tables, direct tables, (m, d/m) in {(32,3), (32,4),
+ *            (16,8), (16,4), (8,12), (8,8)}, nprobe >= 2) and the batch
+ *            probes every list twice or more on average, else by query;
  *          0 by query: one thread block per (query, chunk of its lists);
  *          1 by list where the shapes allow it: the queries that probe a
- *            list are scanned together, `group` of them per table set, each
- *            keeping the codes within the k-th distance of its nearest list
- *            (which is scanned first, by query); a query with more such codes
- *            than its buffer holds is scanned again by query
- *  group  queries per table set of the by-list scan: 2 or 3 (0 keeps the
- *         current value; default 3)
+ *            list are scanned together, up to `group` table sets of them
+ *            per item, each query keeping the codes within a bound taken
+ *            from its nearest list (scanned first); a query with more such
+ *            codes than its buffer holds is scanned again by query
+ *  group  table sets per by-list item: 2 or 3 (a set holds one query's fp32
+ *         tables or two queries' binary16 tables), -1 automatic (default:
+ *         3, or 2 for binary16 tables with m = 16), 0 keeps the current value
  * Errors: INVALID_ARG.
  */
 int ivfpq_set_scan_mode(ivfpq_index* index, int mode, int group);

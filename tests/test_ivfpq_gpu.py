@@ -141,6 +141,37 @@ def test_list_major_scan_follows_the_oracle(B, m, dsub, group):
 
 
 @pytest.mark.parametrize("group", [2, 3])
+@pytest.mark.parametrize("m,dsub", LM_SHAPES)
+def test_list_major_binary16_tables_follow_the_oracle_variant(B, m, dsub, group):
+    """The by-list scan with binary16 tables (two queries' entries per
+    shared-memory word, fp32 sums) against the oracle's binary16 tables, and
+    against the by-query scan's binary16 tables (the general kernel)."""
+    import torch
+    w = S.IVFPQWorkload("t", 260 + m + dsub, 40_000, m * dsub, 61, m, 0.15, True, 300, (9,),
+                        (33,), ("fp16",))
+    data = S.compressed_index(w)
+    q = S.queries(w.number, data.cent, data.weights, w.sigma, w.nq)
+    ix = make_index(B, data.cent, data.cb, data.codes, data.list_ids, data.ids)
+    B.ivfpq_set_lut_type(ix, "fp16")
+    rows = np.arange(0, 300, 5)
+    for k in (1, 100, 700):
+        B.ivfpq_set_scan_mode(ix, 1, group)
+        gp, _ = B.ivfpq_search_probes(ix, _t(q), 9)
+        gd, gi = B.ivfpq_search(ix, _t(q), 9, k)
+        assert B.last_scan_kernel(ix) == "ivfpq_scan_lm_kernel"
+        B.ivfpq_set_scan_mode(ix, 0)
+        qd, qi = B.ivfpq_search(ix, _t(q), 9, k)
+        torch.cuda.synchronize()
+        gp, gd, gi, qd = (t.cpu().numpy() for t in (gp, gd, gi, qd))
+        od, oi, _ = oracle.ivfpq_search(q[rows], data.cent, data.cb, data.list_off, data.codes,
+                                        data.ids, 9, k, oracle.LUT_FP16, forced_probes=gp[rows])
+        assert np.all(np.abs(gd[rows] - od) <= 2e-3 * np.abs(od) + 1e-5), f"k={k}"
+        assert oracle.recall_at_k(gi[rows], oi) >= 0.99
+        # same tables and fp32 sums as the by-query scan, up to summation order
+        assert np.all(np.abs(gd - qd) <= 1e-5 * np.abs(qd) + 1e-6), f"k={k}"
+
+
+@pytest.mark.parametrize("group", [2, 3])
 def test_list_major_candidate_overflow_is_rescanned(B, group):
     """Every query's nearest list holds fewer than k codes, so its bound is
     +inf and all codes of the other probed lists are candidates, more than
