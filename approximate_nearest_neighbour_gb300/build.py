@@ -21,6 +21,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libivfpq_gb300.so"
 LIB_PATH = os.path.join(HERE, LIB_NAME)
+# the debug build: device bounds checks (-DIVFPQ_DEBUG_CHECKS) that record a
+# failure in the device status word instead of trapping
+DEBUG_BUILD_DIR = os.path.join(HERE, "_build_debug")
+DEBUG_LIB_PATH = os.path.join(HERE, "libivfpq_gb300_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
@@ -50,14 +54,18 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build_library(force: bool = False, verbose: bool = False, jobs: int | None = None) -> str:
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build_library(force: bool = False, verbose: bool = False, jobs: int | None = None,
+                  debug: bool = False) -> str:
+    build_dir = DEBUG_BUILD_DIR if debug else BUILD_DIR
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    flags = NVCC_FLAGS + (["-DIVFPQ_DEBUG_CHECKS"] if debug else [])
+    os.makedirs(build_dir, exist_ok=True)
     srcs = _sources()
     hdrs = _headers()
     objs = []
     todo = []
     for src in srcs:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + hdrs):
             todo.append((src, obj))
@@ -65,7 +73,7 @@ def build_library(force: bool = False, verbose: bool = False, jobs: int | None =
 
     def compile_one(item):
         src, obj = item
-        cmd = [exe] + ARCH + NVCC_FLAGS + ["-c", src, "-o", obj + ".tmp"]
+        cmd = [exe] + ARCH + flags + ["-c", src, "-o", obj + ".tmp"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stderr[-4000:]}")
@@ -77,16 +85,16 @@ def build_library(force: bool = False, verbose: bool = False, jobs: int | None =
         n = jobs or max(1, min(len(todo), os.cpu_count() or 1))
         with cf.ThreadPoolExecutor(n) as ex:
             list(ex.map(compile_one, todo))
-    if force or todo or _stale(LIB_PATH, objs):
-        tmp = LIB_PATH + f".{os.getpid()}.tmp"
+    if force or todo or _stale(lib_path, objs):
+        tmp = lib_path + f".{os.getpid()}.tmp"
         cmd = [exe] + ARCH + ["-shared", "-o", tmp] + objs + ["-cudart", "static"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr[-4000:]}")
-        os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     import sys
-    print(build_library(force="--force" in sys.argv, verbose=True))
+    print(build_library(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv))

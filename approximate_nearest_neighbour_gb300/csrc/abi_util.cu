@@ -23,7 +23,8 @@ static std::atomic<unsigned long long> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 // One status word per device, allocated on first use and kept while the
-// library is loaded. Kernels whose bounded waits expire set it to 1.
+// library is loaded. Kernels whose bounded waits expire set bit 0; the
+// debug build's bounds checks set bit 1 and bit 8 + the check's id.
 static std::mutex g_status_mu;
 static int* g_status[64] = {};
 
@@ -56,9 +57,14 @@ extern "C" int ivfpq_device_check(void* stream) {
   if (h != 0) {
     IVFPQ_CUDA(cudaMemsetAsync(w, 0, sizeof(int), s));
     IVFPQ_CUDA(cudaStreamSynchronize(s));
-    set_error("a kernel's bounded wait expired: results of the calls since the last check "
-              "are invalid");
-    return IVFPQ_ERR_TIMEOUT;
+    if (h & 1) {
+      set_error("a kernel's bounded wait expired: results of the calls since the last check "
+                "are invalid");
+      return IVFPQ_ERR_TIMEOUT;
+    }
+    set_error("device bounds checks failed (check mask 0x%x): results of the calls since the "
+              "last check are invalid", unsigned(h) >> 8);
+    return IVFPQ_ERR_DEVICE_CHECK;
   }
   return IVFPQ_OK;
 }

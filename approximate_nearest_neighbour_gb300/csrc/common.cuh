@@ -151,6 +151,22 @@ __device__ __forceinline__ float key_to_float(uint32_t k) {
   return __uint_as_float(k ^ (uint32_t(int32_t(~k) >> 31) | 0x80000000u));
 }
 
+// Device bounds checks of the debug build (-DIVFPQ_DEBUG_CHECKS): dcheck
+// returns ok; when ok is false it records check `id` in the device status
+// word (bit 1 = a check failed, bit 8 + id = which) and the caller skips
+// the access it guards. Kernels never trap or return early on a failed
+// check (their block barriers stay matched); ivfpq_device_check reports
+// IVFPQ_ERR_DEVICE_CHECK. In the normal build the check and its condition
+// compile away.
+#ifdef IVFPQ_DEBUG_CHECKS
+__device__ __forceinline__ bool dcheck(int* word, bool ok, int id) {
+  if (!ok && word) atomicOr(word, 2 | (1 << (8 + id)));
+  return ok;
+}
+#else
+__device__ __forceinline__ bool dcheck(int*, bool, int) { return true; }
+#endif
+
 // Distances produced by the list scan are sums of non-negative terms, so
 // their raw fp32 bits already order correctly as unsigned integers; the
 // sentinel 0xffffffff lies above +inf (0x7f800000).

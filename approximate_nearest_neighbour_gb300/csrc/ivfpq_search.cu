@@ -229,8 +229,11 @@ __global__ void lm_records_kernel(const LmParams p, int G, bool bound_pass, uint
   const int warps = int(gridDim.x) * (blockDim.x >> 5);
   for (int it = int(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5); it < nit; it += warps) {
     const int64_t pos = p.items[it];
-    const int l = p.pair_list[pos];
-    const bool mine = lane < G && pos + lane < p.npairs && p.pair_list[pos + lane] == l;
+    const bool pos_ok = dcheck(sp.dbg, pos >= 0 && pos < p.npairs, 0);
+    const int l = pos_ok ? p.pair_list[pos] : 0;
+    const bool list_ok = dcheck(sp.dbg, l >= 0 && l < sp.nlist, 1);
+    const bool mine = pos_ok && list_ok && lane < G && pos + lane < p.npairs &&
+                      p.pair_list[pos + lane] == l;
     const unsigned vm = __ballot_sync(kFullMask, mine);
     const int nq = __popc(vm);
     uint8_t* rec = records + int64_t(it) * p.rec_bytes;
@@ -238,6 +241,7 @@ __global__ void lm_records_kernel(const LmParams p, int G, bool bound_pass, uint
     int qv = 0;
     if (mine) {
       qv = p.pair_query[pos + lane];
+      if (!dcheck(sp.dbg, qv >= 0 && qv < sp.nq, 2)) qv = 0;
       h->q[lane] = qv;
       h->theta[lane] = bound_pass ? kSentinelKey : p.theta_key[int64_t(qv) * p.theta_stride];
     }
@@ -246,6 +250,7 @@ __global__ void lm_records_kernel(const LmParams p, int G, bool bound_pass, uint
       h->nq = nq;
       h->len = sp.list_len[l];
       h->boff = sp.list_block_off[l];
+      dcheck(sp.dbg, h->boff >= 0 && h->boff + ((h->len + 31) >> 5) <= sp.nblocks, 3);
     }
     float* res = reinterpret_cast<float*>(rec + kLmHead);
     const float* c = sp.centroids + int64_t(l) * sp.d;
@@ -342,7 +347,7 @@ __global__ void lm_final_kernel(const float* __restrict__ pre_d, const int64_t* 
   extern __shared__ uint32_t lmf_smem[];
   const int64_t q = blockIdx.x;
   const int cnt = ccount[q];
-  const int n2 = min(cnt, cap);
+  const int n2 = max(0, min(cnt, cap));
   const int total = k + n2;
   int T = 32;
   while (T < total) T *= 2;
@@ -429,6 +434,11 @@ ScanParams scan_params(const ivfpq_index* ix, const float* queries, int64_t nq, 
   p.nprobe = nprobe;
   p.k = k;
   p.lut_type = ix->lut_type;
+  p.nq = nq;
+  p.nblocks = ix->nblocks;
+#ifdef IVFPQ_DEBUG_CHECKS
+  if (device_status_word(&p.dbg) != IVFPQ_OK) p.dbg = nullptr;
+#endif
   plan_chunks(nq, nprobe, &p.per_chunk, &p.nchunks);
   return p;
 }

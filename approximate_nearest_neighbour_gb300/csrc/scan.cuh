@@ -51,6 +51,9 @@ struct ScanParams {
   int lut_type;              // IVFPQ_LUT_FP32 / FP16 / FP8
   const int* qmask = nullptr;  // if set, only queries q with qmask[q] != 0 are scanned
   const float* term1 = nullptr;  // precomputed list terms [nlist, 256, m] (register-codebook scan)
+  int64_t nq = 0;              // queries of the batch (debug checks)
+  int64_t nblocks = 0;         // code blocks stored (debug checks)
+  int* dbg = nullptr;          // device status word of the debug build, else null
 };
 
 constexpr int kScanWarps = 8;
@@ -357,8 +360,10 @@ ivfpq_scan_kernel(const ScanParams p) {
     __syncthreads();
     if (p.lut_type != IVFPQ_LUT_FP32)
       quantize_lut(scan_smem, lut_words, p.lut_type, &lut_scale, &lut_red, tid);
-    const int len = p.list_len[l];
     const int64_t boff = p.list_block_off[l];
+    const bool in_range = dcheck(
+        p.dbg, boff >= 0 && boff + ((int64_t(p.list_len[l]) + 31) >> 5) <= p.nblocks, 10);
+    const int len = in_range ? p.list_len[l] : 0;
     const int nb = (len + 31) >> 5;
     const uint8_t* lcodes = p.codes + boff * 32 * m;
     if constexpr (MW > 0) {

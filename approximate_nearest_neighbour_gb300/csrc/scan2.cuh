@@ -180,9 +180,12 @@ ivfpq_scan2_kernel(const ScanParams p) {
   for (int i = tid; i < n; i += NW * 32) {
     const int l = p.probes[q * p.nprobe + p0 + i];
     const bool v = l >= 0 && l < p.nlist;
+    const int len = v ? p.list_len[l] : 0;
+    const int64_t boff = v ? p.list_block_off[l] : 0;
+    const bool in_range = dcheck(p.dbg, boff >= 0 && boff + ((len + 31) >> 5) <= p.nblocks, 8);
     s_list[i] = v ? l : -1;
-    s_len[i] = v ? p.list_len[l] : 0;
-    s_boff[i] = v ? p.list_block_off[l] : 0;
+    s_len[i] = in_range ? len : 0;
+    s_boff[i] = boff;
   }
   if constexpr (PRE) {
     // ||x - y_C||^2 of each list, one warp per list (exact form, fp32)
@@ -267,6 +270,7 @@ ivfpq_scan2_kernel(const ScanParams p) {
   ws.finalize();
   // this warp's KW best, ascending (sentinel-padded)
   const int64_t o = ((q * p.nchunks + chunk) * NW + warp) * KW;
+  if (!dcheck(p.dbg, q < p.nq || p.nq == 0, 9)) return;  // after the last barrier
 #pragma unroll
   for (int r = 0; r < KW / 32; ++r) {
     p.pkeys[o + 32 * r + lane] = ws.wk[r];

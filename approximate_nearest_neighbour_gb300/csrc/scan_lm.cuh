@@ -160,7 +160,8 @@ __device__ __forceinline__ void lm_append(const LmParams& p, int q, bool pass, f
   base = __shfl_sync(kFullMask, base, leader);
   if (pass) {
     const int pos = base + __popc(mask & ((1u << lane) - 1u));
-    if (pos < p.cap) {
+    if (pos < p.cap &&
+        dcheck(p.s.dbg, int64_t(slot) < p.s.nblocks * 32 && q >= 0 && q < p.s.nq, 5)) {
       const int64_t o = int64_t(q) * p.cap + pos;
       p.ckey[o] = __float_as_uint(dist);
       p.cid[o] = p.ids[slot];
@@ -265,8 +266,10 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
           word = __float_as_uint(entry(r, s));
         }
         uint32_t* row = tg + e * 64;
+        if (dcheck(sp.dbg, e >= 0 && e < 256, 7)) {
 #pragma unroll
-        for (int rep = 0; rep < REPS; ++rep) row[GS * ((rep + qq) & (REPS - 1))] = word;
+          for (int rep = 0; rep < REPS; ++rep) row[GS * ((rep + qq) & (REPS - 1))] = word;
+        }
       }
     }
   };
@@ -275,7 +278,8 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
   auto first_codes = [&](int slot) {
     const LmHead& d = head(slot);
     const int nb = (d.len + 31) >> 5;
-    if (warp < nb) load_codes<MW>(sp.codes + (d.boff + warp) * 32 * m, lane, c0);
+    const bool in_range = d.boff >= 0 && d.boff + nb <= sp.nblocks;  // checked in scan
+    if (warp < nb && in_range) load_codes<MW>(sp.codes + (d.boff + warp) * 32 * m, lane, c0);
   };
 
   // bound pass: this lane's TQ smallest of the current item, ascending
@@ -299,7 +303,9 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
       qv[g] = g < nqi ? d.q[g] : 0;
       th[g] = g < nqi ? d.theta[g] : 0u;
     }
-    const int nb = (len + 31) >> 5;
+    const bool in_range =
+        dcheck(sp.dbg, boff >= 0 && boff + ((len + 31) >> 5) <= sp.nblocks, 4);
+    const int nb = in_range ? (len + 31) >> 5 : 0;
     const uint8_t* lcodes = sp.codes + boff * 32 * m;
     for (int b = warp; b < nb; b += NW) {
       if (b + NW < nb) load_codes<MW>(lcodes + int64_t(b + NW) * 32 * m, lane, c1);

@@ -51,7 +51,9 @@ def parse():
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--lut", default="fp32", choices=["fp32", "fp16", "fp8"])
+    p.add_argument("--lut", default=None, choices=["fp32", "fp16", "fp8"],
+                   help="lookup-table storage (default: the workload's stated one: fp32, "
+                        "binary16 for billion)")
     p.add_argument("--n", type=int, default=None, help="database size override (development)")
     p.add_argument("--nq", type=int, default=None)
     p.add_argument("--nlist", type=int, default=None, help="list count override (development)")
@@ -710,6 +712,10 @@ def main():
     global WORKLOAD, NPROBE, K
     args = parse()
     WORKLOAD, NPROBE, K = WORKLOADS[args.workload]
+    if args.lut is None:
+        # the billion workload states binary16 tables; the others fp32 (the
+        # large workload's fp16 / E4M3 variants are recall-gated in the tests)
+        args.lut = "fp16" if args.workload == "billion" else "fp32"
     if args.k is not None:
         K = args.k
     if args.workload == "kselect":
