@@ -47,6 +47,7 @@ SIGNATURES = {
     "ivfpq_set_scan_mode": (_I, [_VP, _I, _I]),
     "ivfpq_uses_precomputed": (_I, [_VP]),
     "ivfpq_kernel_launches": (C.c_uint64, []),
+    "ivfpq_workspace_allocations": (C.c_uint64, []),
     "flat_knn": (_I, [_VP, _I64, _I, _VP, _I64, _I, _VP, _VP, _VP]),
     "kselect": (_I, [_VP, _I64, _I64, _I, _VP, _VP, _VP]),
     "kselect_noalloc": (_I, [_VP, _I64, _I64, _I, _VP, _VP, _VP]),
@@ -316,6 +317,11 @@ def last_scan_kernel(index):
 def kernel_launches():
     """Kernels launched by the library since it was loaded."""
     return int(lib().ivfpq_kernel_launches())
+
+
+def workspace_allocations():
+    """Temporary device allocations the library has made since it was loaded."""
+    return int(lib().ivfpq_workspace_allocations())
 
 
 def device_check(stream=None):

@@ -22,6 +22,9 @@ void clear_error() { g_err[0] = 0; }
 static std::atomic<unsigned long long> g_launches{0};
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+static std::atomic<unsigned long long> g_ws_allocs{0};
+void count_workspace_alloc() { g_ws_allocs.fetch_add(1, std::memory_order_relaxed); }
+
 // One status word per device, allocated on first use and kept while the
 // library is loaded. Kernels whose bounded waits expire set bit 0; the
 // debug build's bounds checks set bit 1 and bit 8 + the check's id.
@@ -72,6 +75,8 @@ extern "C" int ivfpq_device_check(void* stream) {
 extern "C" const char* ivfpq_last_error(void) { return ivfpq::g_err; }
 
 extern "C" uint64_t ivfpq_kernel_launches(void) { return ivfpq::g_launches.load(); }
+
+extern "C" uint64_t ivfpq_workspace_allocations(void) { return ivfpq::g_ws_allocs.load(); }
 
 extern "C" const char* ivfpq_status_string(int status) {
   switch (status) {

@@ -43,6 +43,8 @@ void clear_error();
 
 // Number of kernels this library has launched (all threads, all devices).
 void count_launch();
+// Number of workspace allocations the library has made (all threads).
+void count_workspace_alloc();
 
 // Checks (and counts) the launch that was just enqueued.
 #define IVFPQ_LAUNCHED()             \
@@ -94,6 +96,7 @@ class Workspace {
                 cudaGetErrorString(e));
       return IVFPQ_ERR_OOM;
     }
+    count_workspace_alloc();
     p_[n_++] = p;
     *out = static_cast<T*>(p);
     return IVFPQ_OK;

@@ -233,6 +233,11 @@ const char* ivfpq_last_scan_kernel(const ivfpq_index* index);
  * since it was loaded (all threads); a measurement aid. */
 uint64_t ivfpq_kernel_launches(void);
 
+/* ivfpq_workspace_allocations -- number of temporary device allocations
+ * (stream-ordered workspace) the library has made since it was loaded (all
+ * threads); lets a caller check that an entry point allocated nothing. */
+uint64_t ivfpq_workspace_allocations(void);
+
 /*
  * flat_knn -- exact brute-force k-NN under squared L2.
  * Source: exact search by a GEMM-form distance ||x||^2 - 2<x, y> + ||y||^2

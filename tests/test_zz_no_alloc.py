@@ -29,6 +29,10 @@ def _compare(vals, k, ref_v, ref_i, got_v, got_i):
 
 
 def test_kselect_noalloc_matches_kselect_on_two_calls_in_a_row():
+    """Two different problems back to back (leftovers of the first in the
+    shared array must not reach the second); the library's count of its own
+    temporary allocations does not move during the calls, while kselect on
+    the same problem does allocate (so the count would show it)."""
     import torch
     from approximate_nearest_neighbour_gb300 import binding as B
 
@@ -36,13 +40,37 @@ def test_kselect_noalloc_matches_kselect_on_two_calls_in_a_row():
     for seed, (rows, cols, k) in enumerate([(3, 1_000_003, 100), (2, 600_000, 1000)]):
         vals = S.random_rows(rows, cols, seed=40 + seed)
         t = torch.from_numpy(vals).cuda()
+        a0 = B.workspace_allocations()
         ref_v, ref_i = B.kselect(t, k)
+        torch.cuda.synchronize()
+        assert B.workspace_allocations() > a0  # kselect takes its partials from the pool
         got_v = torch.empty((rows, k), dtype=torch.float32, device="cuda")
         got_i = torch.empty((rows, k), dtype=torch.int64, device="cuda")
+        a1 = B.workspace_allocations()
         B.kselect_noalloc(t, k, got_v, got_i)
         torch.cuda.synchronize()
+        assert B.workspace_allocations() == a1  # no allocation
         _compare(vals, k, ref_v.cpu().numpy(), ref_i.cpu().numpy(), got_v.cpu().numpy(),
                  got_i.cpu().numpy())
+
+
+def test_kselect_noalloc_matches_the_oracle():
+    """One case against the oracle's k-selection (a stable full sort)."""
+    import torch
+    import oracle
+    from approximate_nearest_neighbour_gb300 import binding as B
+
+    rows, cols, k = 2, 300_001, 64
+    vals = S.random_rows(rows, cols, seed=77)
+    t = torch.from_numpy(vals).cuda()
+    got_v = torch.empty((rows, k), dtype=torch.float32, device="cuda")
+    got_i = torch.empty((rows, k), dtype=torch.int64, device="cuda")
+    a0 = B.workspace_allocations()
+    B.kselect_noalloc(t, k, got_v, got_i)
+    torch.cuda.synchronize()
+    assert B.workspace_allocations() == a0
+    ref_v, ref_i = oracle.kselect(vals, k)
+    _compare(vals, k, ref_v, ref_i, got_v.cpu().numpy(), got_i.cpu().numpy())
 
 
 def test_kselect_noalloc_rejects_problems_beyond_its_scratch():
