@@ -108,6 +108,23 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
+// 32 consecutive accumulator columns of the warp's 32 TMEM lanes into
+// registers, without waiting for the load (tmem_wait_ld does).
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
@@ -328,6 +345,55 @@ l2_tc_kernel(const __grid_constant__ CUtensorMap mq_hi, const __grid_constant__ 
       }
       tc_fence_after();
       const int col0 = (t0 + i) * TN;
+      if constexpr (MODE == kModeFilter) {
+        if (col0 + TN <= a.n) {
+          // a full tile: both accumulator chunks of this half loaded before one
+          // wait; lane j holds the norm of column j of each chunk and hands it
+          // to the other lanes by shuffle; four partial pass masks keep the
+          // compare chain short; a warp with no passing entry skips the appends
+          uint32_t r0[32], r1[32];
+          const uint32_t ta = tmem + (uint32_t(32 * lg) << 16) + uint32_t(ab * TN + half * 64);
+          tmem_ld32_nowait(ta, r0);
+          tmem_ld32_nowait(ta + 32, r1);
+          const int cb0 = col0 + half * 64;
+          const float xr0 = __ldg(a.xnorm + cb0 + lane);
+          const float xr1 = __ldg(a.xnorm + cb0 + 32 + lane);
+          tmem_wait_ld();
+          uint32_t m0[4] = {0, 0, 0, 0}, m1[4] = {0, 0, 0, 0};
+          float u0[32], u1[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            u0[j] = fmaf(-2.f, __uint_as_float(r0[j]), __shfl_sync(kFullMask, xr0, j));
+            u1[j] = fmaf(-2.f, __uint_as_float(r1[j]), __shfl_sync(kFullMask, xr1, j));
+            m0[j & 3] |= uint32_t(u0[j] <= bnd) << j;
+            m1[j & 3] |= uint32_t(u1[j] <= bnd) << j;
+          }
+          const uint32_t mk0 = (m0[0] | m0[1]) | (m0[2] | m0[3]);
+          const uint32_t mk1 = (m1[0] | m1[1]) | (m1[2] | m1[3]);
+          if (__any_sync(kFullMask, (mk0 | mk1) != 0u)) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if ((mk0 >> j) & 1u) {
+                if (cnt < a.cap_s)
+                  seg[cnt] = (uint64_t(float_to_key(u0[j] + qn)) << 32) | uint32_t(cb0 + j);
+                ++cnt;
+              }
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if ((mk1 >> j) & 1u) {
+                if (cnt < a.cap_s)
+                  seg[cnt] = (uint64_t(float_to_key(u1[j] + qn)) << 32) | uint32_t(cb0 + 32 + j);
+                ++cnt;
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_acce(ab));
+          continue;
+        }
+      }
 #pragma unroll
       for (int cc = 0; cc < NC; ++cc) {
         const int c = half * NC + cc;

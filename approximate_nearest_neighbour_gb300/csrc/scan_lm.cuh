@@ -258,8 +258,9 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
         const int e = (s * NW + warp) * QQ + qq;
         uint32_t word;
         if constexpr (H) {
+          // a missing second query gets +inf entries: its sums never pass
           const float T0 = entry(r, s);
-          const float T1 = two ? entry(r2, s) : 0.f;
+          const float T1 = two ? entry(r2, s) : INFINITY;
           word = uint32_t(__half_as_ushort(__float2half_rn(T0))) |
                  (uint32_t(__half_as_ushort(__float2half_rn(T1))) << 16);
         } else {
@@ -300,8 +301,12 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
     uint32_t th[GG];
 #pragma unroll
     for (int g = 0; g < GG; ++g) {
-      qv[g] = g < nqi ? d.q[g] : 0;
-      th[g] = g < nqi ? d.theta[g] : 0u;
+      // fp32 items are scanned with exactly their query count (GG = nqi);
+      // binary16 ones in whole pairs, so the last pair may have one query:
+      // the missing one has +inf table entries and bound 0, so nothing passes
+      const bool live = !H || g < nqi;
+      qv[g] = live ? d.q[g] : d.q[0];
+      th[g] = live ? d.theta[g] : 0u;
     }
     const bool in_range =
         dcheck(sp.dbg, boff >= 0 && boff + ((len + 31) >> 5) <= sp.nblocks, 4);
@@ -331,7 +336,7 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
               tq[i] = max(a, b);
             }
           }
-        } else if (g < nqi) {
+        } else {
           lm_append(p, qv[g], valid && __float_as_uint(dist) <= th[g], dist, slot_id, lane);
         }
       }
