@@ -407,10 +407,13 @@ def run_ours(args):
         scan_ms = sums[2] / max(count, 1)
         achieved = scan_bytes / (scan_ms / 1e3) / 1e9
         traffic = profiled_traffic(scan_kernel)
-        # the look-up bound: one shared-memory word per code byte
+        # the look-up bound: one 4-byte shared-memory word per code byte and
+        # query, or per two queries where the by-list scan packs two binary16
+        # entries into a word
         nsm = torch.cuda.get_device_properties(dev).multi_processor_count
         sm_mhz = sm_max_mhz()
-        lookup_peak = nsm * LOOKUPS_PER_SM_CLOCK * sm_mhz * 1e6
+        per_word = 2 if (args.lut == "fp16" and scan_kernel == "ivfpq_scan_lm_kernel") else 1
+        lookup_peak = nsm * LOOKUPS_PER_SM_CLOCK * per_word * sm_mhz * 1e6
         lookups_per_s = scan_bytes / (scan_ms / 1e3)
         if traffic is not None and (args.n is not None or args.nlist is not None
                                     or args.workload != "large"):
@@ -435,6 +438,7 @@ def run_ours(args):
                                 "achieved": lookups_per_s / 1e12, "unit": "Tlookups/s",
                                 "peak": lookup_peak / 1e12, "frac": lookups_per_s / lookup_peak,
                                 "peak_source": f"{nsm} SMs x {LOOKUPS_PER_SM_CLOCK} banks x "
+                                               f"{per_word} entries per word x "
                                                f"{sm_mhz:.0f} MHz"},
             "stage_ms": {"coarse": sums[0] / max(count, 1), "plan": sums[1] / max(count, 1),
                          "scan": scan_ms, "merge": sums[3] / max(count, 1)},
