@@ -247,6 +247,7 @@ __global__ void lm_records_kernel(const LmParams p, int G, bool bound_pass, uint
     }
     if (lane == 0) {
       h->list = l;
+      h->item = it;
       h->nq = nq;
       h->len = sp.list_len[l];
       h->boff = sp.list_block_off[l];
@@ -316,12 +317,68 @@ __global__ void lm_items_kernel(const int32_t* __restrict__ flag, const int32_t*
 // theta[r] = the k-th smallest of row r's len keys (the sentinel when fewer
 // than k keys are below it): one warp per row, a binary search over the
 // 32-bit key range for the least v with at least k keys <= v.
-__global__ void lm_theta_kernel(const uint32_t* __restrict__ keys, int64_t rows, int len, int k,
-                                uint32_t* __restrict__ theta) {
+// The bound pass scans each query's nearest list in chunks of `chunk` codes
+// (a multiple of 32), one item per chunk, so that a long list (the largest of
+// a Zipf mixture holds ~1e6 codes) is spread over several blocks.
+constexpr int kBoundChunkMin = 32768;
+constexpr int kBoundChunksMax = 4;
+
+// cnt[q] = chunks of query q's nearest list (at least 1)
+__global__ void bound_chunks_kernel(const int32_t* __restrict__ probes, int64_t nq, int nprobe,
+                                    const int32_t* __restrict__ list_len, int nlist, int chunk,
+                                    int32_t* __restrict__ cnt) {
+  const int64_t q = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (q >= nq) return;
+  const int l = probes[q * nprobe];
+  const int len = (l >= 0 && l < nlist) ? list_len[l] : 0;
+  cnt[q] = max(1, (len + chunk - 1) / chunk);
+}
+
+// Records of the bound pass (one warp per query, one record per chunk of its
+// nearest list, at item off[q] + c); *n_items = the number of items.
+__global__ void bound_records_kernel(const LmParams p, int nprobe, int chunk,
+                                     const int32_t* __restrict__ off,
+                                     const int32_t* __restrict__ cnt, uint8_t* records,
+                                     int* __restrict__ n_items) {
+  const ScanParams& sp = p.s;
+  const int lane = threadIdx.x & 31;
+  const int64_t q = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (q >= sp.nq) return;  // the same for the whole warp
+  if (q == sp.nq - 1 && lane == 0) *n_items = off[q] + cnt[q];
+  const int l0 = sp.probes[q * nprobe];
+  const bool valid = dcheck(sp.dbg, l0 >= -1 && l0 < sp.nlist, 1) && l0 >= 0 && l0 < sp.nlist;
+  const int l = valid ? l0 : 0;
+  const int total = valid ? sp.list_len[l] : 0;
+  const int64_t boff = sp.list_block_off[l];
+  const float* x = sp.queries + q * sp.d;
+  const float* c = sp.centroids + int64_t(l) * sp.d;
+  for (int ch = 0; ch < cnt[q]; ++ch) {
+    const int it = off[q] + ch;
+    uint8_t* rec = records + int64_t(it) * p.rec_bytes;
+    if (lane == 0) {
+      LmHead* h = reinterpret_cast<LmHead*>(rec);
+      h->list = l;
+      h->item = it;
+      h->nq = 1;
+      h->len = max(0, min(chunk, total - ch * chunk));
+      h->boff = boff + int64_t(ch) * (chunk / 32);
+      h->q[0] = int(q);
+      h->theta[0] = kSentinelKey;
+    }
+    float* res = reinterpret_cast<float*>(rec + kLmHead);
+    for (int t = lane; t < p.dpad; t += 32) res[t] = t < sp.d ? x[t] - c[t] : 0.f;
+  }
+}
+
+// Row r holds cnt[r] * per keys from keys + off[r] * per.
+__global__ void lm_theta_kernel(const uint32_t* __restrict__ keys, int64_t rows,
+                                const int32_t* __restrict__ off, const int32_t* __restrict__ cnt,
+                                int per, int k, uint32_t* __restrict__ theta) {
   const int lane = threadIdx.x & 31;
   const int64_t row = int64_t(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (row >= rows) return;  // the same for the whole warp
-  const uint32_t* kr = keys + row * len;
+  const uint32_t* kr = keys + int64_t(off[row]) * per;
+  const int len = cnt[row] * per;
   uint32_t lo = 0, hi = kSentinelKey;
   while (lo < hi) {
     const uint32_t mid = lo + ((hi - lo) >> 1);
@@ -610,17 +667,41 @@ int scan_stage_lm(const ivfpq_index* ix, const float* queries, int64_t nq, int n
   auto* mix = const_cast<ivfpq_index*>(ix);
   Workspace ws(s);
   const ScanParams base = scan_params(ix, queries, nq, nprobe, probes, k);
-  // 1. bound pass: per query, 512 lane queues of tq over its nearest list
-  //    (512 * tq >= 2k), and the k-th smallest of their entries
+  // 1. bound pass: per query and chunk of its nearest list, 512 lane queues
+  //    of tq (512 * tq >= 2k), and the k-th smallest of their entries
   const int tq = k <= 512 ? 2 : k <= 1024 ? 4 : 8;
   LmParams bp;
   bp.s = base;
-  IVFPQ_TRY(plan_items(probes, nq, nprobe, 0, 1, 1, ix->nlist, ws, s, bp));
-  IVFPQ_TRY(make_records(bp, 1, true, ws, s));
-  const int64_t plen = int64_t(kLmWarps) * 32 * tq;
-  const size_t npart = size_t(nq) * plen;
-  IVFPQ_TRY(ws.alloc(&bp.part_key, npart));
-  IVFPQ_CUDA(cudaMemsetAsync(bp.part_key, 0xff, npart * sizeof(uint32_t), s));
+  int32_t *bcnt = nullptr, *boffs = nullptr;
+  int* bn_items = nullptr;
+  IVFPQ_TRY(ws.alloc(&bcnt, size_t(nq)));
+  IVFPQ_TRY(ws.alloc(&boffs, size_t(nq)));
+  IVFPQ_TRY(ws.alloc(&bn_items, 1));
+  // chunks of at least 32,768 codes, at most 4 per query
+  int64_t chunk = std::max<int64_t>(kBoundChunkMin, ceil_div(ix->max_list_len, kBoundChunksMax));
+  chunk = ceil_div(chunk, 32) * 32;
+  IVFPQ_REQUIRE(chunk < (int64_t(1) << 30), "scan: list of %lld vectors", (long long)ix->max_list_len);
+  bound_chunks_kernel<<<unsigned(ceil_div(nq, 256)), 256, 0, s>>>(probes, nq, nprobe, ix->list_len,
+                                                                 ix->nlist, int(chunk), bcnt);
+  IVFPQ_LAUNCHED();
+  {
+    size_t sb = 0;
+    IVFPQ_CUDA(cub::DeviceScan::ExclusiveSum(nullptr, sb, bcnt, boffs, nq, s));
+    uint8_t* st = nullptr;
+    IVFPQ_TRY(ws.alloc(&st, sb));
+    IVFPQ_CUDA(cub::DeviceScan::ExclusiveSum(st, sb, bcnt, boffs, nq, s));
+  }
+  const int64_t max_items = nq * std::max<int64_t>(1, ceil_div(ix->max_list_len, chunk));
+  bp.dpad = (base.d + 3) & ~3;
+  bp.rec_bytes = lm_record_bytes(1, base.d);
+  bp.n_items = bn_items;
+  IVFPQ_TRY(ws.alloc(&bp.records_w, size_t(max_items) * bp.rec_bytes));
+  bp.records = bp.records_w;
+  bound_records_kernel<<<unsigned(ceil_div(nq, 8)), 256, 0, s>>>(bp, nprobe, int(chunk), boffs,
+                                                                bcnt, bp.records_w, bn_items);
+  IVFPQ_LAUNCHED();
+  const int64_t plen = int64_t(kLmWarps) * 32 * tq;  // keys per item
+  IVFPQ_TRY(ws.alloc(&bp.part_key, size_t(max_items) * plen));
   int launched = 0;
   const bool half = ix->lut_type == IVFPQ_LUT_FP16;
   if (half) IVFPQ_TRY(launch_bound_pass<IVFPQ_LUT_FP16>(bp, tq, s, &launched));
@@ -628,7 +709,8 @@ int scan_stage_lm(const ivfpq_index* ix, const float* queries, int64_t nq, int n
   IVFPQ_REQUIRE(launched, "scan: no list-major kernel for m=%d d/m=%d", ix->m, ix->dsub);
   uint32_t* theta = nullptr;
   IVFPQ_TRY(ws.alloc(&theta, size_t(nq)));
-  lm_theta_kernel<<<unsigned(ceil_div(nq, 8)), 256, 0, s>>>(bp.part_key, nq, int(plen), k, theta);
+  lm_theta_kernel<<<unsigned(ceil_div(nq, 8)), 256, 0, s>>>(bp.part_key, nq, boffs, bcnt,
+                                                            int(plen), k, theta);
   IVFPQ_LAUNCHED();
   // 2. filter pass over all the probed lists
   LmParams lp;

@@ -26,12 +26,15 @@
 //    candidates are the query's result, and a query whose buffer overflows
 //    is scanned again by the general kernel;
 //  * the bound comes from a first pass of the same kernel over every query's
-//    nearest list alone (one query per item, TQ > 0): each lane keeps the TQ
-//    smallest distances of the codes it scores (a sorted register queue, no
-//    communication between lanes) and writes them out; the k-th smallest of
-//    those 512 * TQ distances (512 * TQ >= k) is at least the k-th smallest
-//    of the list (a lane that saw more than TQ of the list's k smallest only
-//    makes it larger), hence at least the query's final k-th distance.
+//    nearest list alone (TQ > 0; one item per query and chunk of that list,
+//    the chunks at least 32,768 codes long and at most 4 per list, so a long
+//    list is spread over blocks): each lane keeps the TQ smallest distances
+//    of the codes it scores (a sorted register queue, no communication
+//    between lanes) and writes them out; the k-th smallest of the query's
+//    512 * TQ distances per chunk (512 * TQ >= k) is at least the k-th
+//    smallest of the list (a lane that saw more than TQ of the list's k
+//    smallest only makes it larger), hence at least the query's final k-th
+//    distance.
 #pragma once
 
 #include <type_traits>
@@ -60,11 +63,12 @@ struct LmParams {
   int64_t* cid;                // [nq, cap] candidate ids
   int* ccount;                 // [nq] candidates appended (may exceed cap)
   int cap;
-  // bound pass: lane i of warp w's TQ smallest distances for query q at
-  // part_key[((q * 16 + w) * 32 + i) * TQ ..], ascending, sentinel-padded
+  // bound pass: lane i of warp w's TQ smallest distances for item it at
+  // part_key[((it * 16 + w) * 32 + i) * TQ ..], ascending, sentinel-padded
   uint32_t* part_key;
-  // item records (lm_records_kernel): rec_bytes each
+  // item records (lm_records_kernel, bound_records_kernel): rec_bytes each
   const uint8_t* records;
+  uint8_t* records_w = nullptr;  // the same, for the kernels that write them
   int rec_bytes;
   int dpad;                    // d rounded up to a multiple of 4
 };
@@ -72,7 +76,7 @@ struct LmParams {
 // Head of an item record; the G residuals x_q - c_list (dpad floats each)
 // follow at byte kLmHead.
 struct LmHead {
-  int list, len, nq, pad;
+  int list, len, nq, item;  // item: its index (the bound pass writes by item)
   int64_t boff;
   int q[kLmMaxG];
   uint32_t theta[kLmMaxG];
@@ -344,7 +348,7 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
       for (int w = 0; w < MW; ++w) c0[w] = c1[w];
     }
     if constexpr (TQ > 0) {
-      uint32_t* o = p.part_key + ((int64_t(qv[0]) * NW + warp) * 32 + lane) * TQ;
+      uint32_t* o = p.part_key + ((int64_t(d.item) * NW + warp) * 32 + lane) * TQ;
 #pragma unroll
       for (int i = 0; i < TQ; ++i) {
         o[i] = tq[i];

@@ -171,6 +171,41 @@ def test_list_major_binary16_tables_follow_the_oracle_variant(B, m, dsub, group)
         assert np.all(np.abs(gd - qd) <= 1e-5 * np.abs(qd) + 1e-6), f"k={k}"
 
 
+@pytest.mark.parametrize("lut", ["fp32", "fp16"])
+def test_list_major_long_nearest_list_is_chunked(B, lut):
+    """A nearest list longer than a bound-pass chunk (32,768 codes): its
+    chunks are separate items whose lane queues together give the bound."""
+    import torch
+    rng = np.random.default_rng(91)
+    nlist, m, dsub = 8, 8, 12
+    d = m * dsub
+    cent = (3 * rng.standard_normal((nlist, d))).astype(np.float32)
+    cb = (0.3 * rng.standard_normal((m, 256, dsub))).astype(np.float32)
+    sizes = [100_003, 700, 650, 600, 550, 500, 450, 400]
+    list_ids = np.repeat(np.arange(nlist, dtype=np.int32), sizes)
+    n = list_ids.shape[0]
+    codes = rng.integers(0, 256, (n, m)).astype(np.uint8)
+    ids = np.arange(n, dtype=np.int64) * 3 + 1
+    ix = make_index(B, cent, cb, codes, list_ids, ids)
+    B.ivfpq_set_lut_type(ix, lut)
+    B.ivfpq_set_scan_mode(ix, 1)
+    q = (cent[0] + 0.05 * rng.standard_normal((48, d))).astype(np.float32)
+    q[40:] = cent[3] + 0.05 * rng.standard_normal((8, d))  # some with a short nearest list
+    lists = oracle.to_lists(codes, list_ids, ids, nlist)
+    for k in (10, 100, 1000):
+        if lut == "fp32":
+            search_and_check(B, ix, cent, cb, lists, q, 4, k, context=f"chunked k={k}")
+        else:
+            gp, _ = B.ivfpq_search_probes(ix, _t(q), 4)
+            gd, gi = B.ivfpq_search(ix, _t(q), 4, k)
+            torch.cuda.synchronize()
+            gp, gd, gi = gp.cpu().numpy(), gd.cpu().numpy(), gi.cpu().numpy()
+            od, oi, _ = oracle.ivfpq_search(q, cent, cb, lists[0], lists[1], lists[2], 4, k,
+                                            oracle.LUT_FP16, forced_probes=gp)
+            assert np.all(np.abs(gd - od) <= 2e-3 * np.abs(od) + 1e-5), f"k={k}"
+        assert B.last_scan_kernel(ix) == "ivfpq_scan_lm_kernel"
+
+
 @pytest.mark.parametrize("group", [2, 3])
 def test_list_major_candidate_overflow_is_rescanned(B, group):
     """Every query's nearest list holds fewer than k codes, so its bound is
