@@ -103,7 +103,7 @@ class Workspace {
   }
 
  private:
-  static const int kMax = 32;
+  static const int kMax = 48;
   cudaStream_t s_;
   void* p_[kMax];
   int n_ = 0;

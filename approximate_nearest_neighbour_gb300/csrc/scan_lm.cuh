@@ -69,6 +69,8 @@ struct LmParams {
   // item records (lm_records_kernel, bound_records_kernel): rec_bytes each
   const uint8_t* records;
   uint8_t* records_w = nullptr;  // the same, for the kernels that write them
+  // the kernel's i-th item is record order[i] (null: record i)
+  const int32_t* order = nullptr;
   int rec_bytes;
   int dpad;                    // d rounded up to a multiple of 4
 };
@@ -152,6 +154,12 @@ __device__ __forceinline__ void lm_lookups_h(const uint32_t (&w)[MW], const char
   }
 }
 
+// Per-query partial sums of one code block (acc[q][s & 3] over positions s).
+template <int NA>
+struct LmAcc {
+  float v[NA][4];
+};
+
 // Appends (dist, id of slot) to query q's candidates where `pass` holds.
 // All 32 lanes call it together.
 __device__ __forceinline__ void lm_append(const LmParams& p, int q, bool pass, float dist,
@@ -171,6 +179,15 @@ __device__ __forceinline__ void lm_append(const LmParams& p, int q, bool pass, f
       p.cid[o] = p.ids[slot];
     }
   }
+}
+
+// Code blocks in flight per warp. The bound pass (one query per item, a few
+// look-ups per code) gains from a deep ring with short codes; the filter
+// pass does not: billion (m = 8, binary16) planning / filter ms at 10,000
+// queries, depth 2: 1.34 / 12.03, bound 8: 0.90, filter 3: 12.88, filter 4:
+// 14.59; mid (m = 16) filter 6.05 at 2, 7.01 at 3 (with register spills).
+__host__ __device__ constexpr int lm_prefetch_depth(int MW, int TQ) {
+  return TQ > 0 && MW < 8 ? 16 / MW : 2;
 }
 
 template <int MW, int DS, int G, int TQ, int LT>
@@ -222,7 +239,7 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
   // before the barrier that ends the iteration
   auto fetch = [&](int it, int slot) {
     if (warp != 0 || it >= nit) return;
-    const uint8_t* src = p.records + int64_t(it) * p.rec_bytes;
+    const uint8_t* src = p.records + int64_t(p.order ? p.order[it] : it) * p.rec_bytes;
     uint8_t* dst = slots + slot * p.rec_bytes;
     for (int c = lane; c < p.rec_bytes / 16; c += 32) lm_cp_async16(dst + 16 * c, src + 16 * c);
     asm volatile("cp.async.commit_group;" ::: "memory");
@@ -279,12 +296,24 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
     }
   };
 
-  uint32_t c0[MW], c1[MW];
+  // code blocks in flight per warp: PD = 2 is a double buffer (block b is
+  // scored while b + NW loads, then copied over); PD > 2 a ring of PD blocks
+  // (b, b + NW, ..., b + (PD-1) NW) whose slot is refilled with the block PD NW
+  // further on as soon as its look-ups have read it, so PD - 1 loads overlap
+  // each block's scoring (with short codes and few look-ups per code, one
+  // load in flight does not cover the memory latency); the ring's unrolled
+  // loop spills where the double buffer does not (m = 32)
+  constexpr int PD = lm_prefetch_depth(MW, TQ);
+  constexpr int PF = PD == 2 ? 1 : PD;  // blocks loaded before the scan
+  uint32_t cr[PD][MW];
   auto first_codes = [&](int slot) {
     const LmHead& d = head(slot);
     const int nb = (d.len + 31) >> 5;
     const bool in_range = d.boff >= 0 && d.boff + nb <= sp.nblocks;  // checked in scan
-    if (warp < nb && in_range) load_codes<MW>(sp.codes + (d.boff + warp) * 32 * m, lane, c0);
+#pragma unroll
+    for (int u = 0; u < PF; ++u)
+      if (warp + u * NW < nb && in_range)
+        load_codes<MW>(sp.codes + (d.boff + warp + u * NW) * 32 * m, lane, cr[u]);
   };
 
   // bound pass: this lane's TQ smallest of the current item, ascending
@@ -316,36 +345,55 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
         dcheck(sp.dbg, boff >= 0 && boff + ((len + 31) >> 5) <= sp.nblocks, 4);
     const int nb = in_range ? (len + 31) >> 5 : 0;
     const uint8_t* lcodes = sp.codes + boff * 32 * m;
-    for (int b = warp; b < nb; b += NW) {
-      if (b + NW < nb) load_codes<MW>(lcodes + int64_t(b + NW) * 32 * m, lane, c1);
-      constexpr int NA = H ? 2 * ((GG + 1) / 2) : GG;
-      float acc[NA][4];
+    // partial sums of a code block from its code words w
+    auto score = [&](const uint32_t (&w)[MW]) {
+      LmAcc<H ? 2 * ((GG + 1) / 2) : GG> acc;
 #pragma unroll
-      for (int g = 0; g < NA; ++g) acc[g][0] = acc[g][1] = acc[g][2] = acc[g][3] = 0.f;
-      if constexpr (H) lm_lookups_h<MW, (GG + 1) / 2, (GG > 4 ? 2 : 4), P>(c0, tab_bytes, lcol, acc);
-      else lm_lookups<MW, GG, P>(c0, tab_bytes, lcol, acc);
+      for (auto& a : acc.v) a[0] = a[1] = a[2] = a[3] = 0.f;
+      if constexpr (H) lm_lookups_h<MW, (GG + 1) / 2, (GG > 4 ? 2 : 4), P>(w, tab_bytes, lcol, acc.v);
+      else lm_lookups<MW, GG, P>(w, tab_bytes, lcol, acc.v);
+      return acc;
+    };
+    auto select = [&](const auto& acc, int b) {
       const bool valid = b * 32 + lane < len;
       const uint32_t slot_id = uint32_t((boff + b) * 32 + lane);
 #pragma unroll
       for (int g = 0; g < GG; ++g) {
-        const float dist = (acc[g][0] + acc[g][1]) + (acc[g][2] + acc[g][3]);
+        const float dist = (acc.v[g][0] + acc.v[g][1]) + (acc.v[g][2] + acc.v[g][3]);
         if constexpr (TQ > 0) {
           const uint32_t key = valid ? __float_as_uint(dist) : kSentinelKey;
           if (key < tq[TQ - 1]) {
             tq[TQ - 1] = key;
 #pragma unroll
             for (int i = TQ - 1; i > 0; --i) {
-              const uint32_t a = tq[i - 1], b = tq[i];
-              tq[i - 1] = min(a, b);
-              tq[i] = max(a, b);
+              const uint32_t lo = tq[i - 1], hi = tq[i];
+              tq[i - 1] = min(lo, hi);
+              tq[i] = max(lo, hi);
             }
           }
         } else {
           lm_append(p, qv[g], valid && __float_as_uint(dist) <= th[g], dist, slot_id, lane);
         }
       }
+    };
+    if constexpr (PD == 2) {
+      for (int b = warp; b < nb; b += NW) {
+        if (b + NW < nb) load_codes<MW>(lcodes + int64_t(b + NW) * 32 * m, lane, cr[1]);
+        select(score(cr[0]), b);
 #pragma unroll
-      for (int w = 0; w < MW; ++w) c0[w] = c1[w];
+        for (int w = 0; w < MW; ++w) cr[0][w] = cr[1][w];
+      }
+    } else {
+      for (int b0 = warp; b0 < nb; b0 += PD * NW) {
+#pragma unroll
+        for (int u = 0; u < PD; ++u) {
+          const int b = b0 + u * NW;
+          if (b >= nb) break;  // the same for the whole warp
+          const auto acc = score(cr[u]);
+          if (b + PD * NW < nb) load_codes<MW>(lcodes + int64_t(b + PD * NW) * 32 * m, lane, cr[u]);
+          select(acc, b);
+        }
+      }
     }
     if constexpr (TQ > 0) {
       uint32_t* o = p.part_key + ((int64_t(d.item) * NW + warp) * 32 + lane) * TQ;
