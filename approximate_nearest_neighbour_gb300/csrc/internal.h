@@ -113,6 +113,9 @@ int select_candidates(const uint64_t* cand, const int* scnt, int nseg, int cap_s
 // construction (ivfpq_index.cu).
 bool use_precomputed(const ivfpq_index* ix);
 int build_term1(ivfpq_index* ix);
+// unit_len and unit_extra of the index from its list lengths
+// (ivfpq_search.cu; called whenever the lists change).
+void update_list_units(ivfpq_index* ix);
 
 // ---- flat / coarse search on distance tiles (flat.cu) ----------------------------
 // k nearest rows of X for each row of Q under squared L2; output as SelectOut
@@ -153,6 +156,10 @@ struct ivfpq_index {
   int64_t* ids = nullptr;             // [nblocks * 32], -1 on padding slots
   std::vector<int64_t> h_list_len;    // host mirror of list_len
   int64_t max_list_len = 0;
+  // by-list filter pass: lists longer than unit_len codes are scanned in
+  // chunks of unit_len (0: no list is); unit_extra = the sum over lists of
+  // their chunks beyond the first (set by ivfpq::update_list_units)
+  int64_t unit_len = 0, unit_extra = 0;
   // queries re-scanned with full-length queues since the last read
   // (ivfpq_repaired_queries); device int64
   unsigned long long* repaired = nullptr;

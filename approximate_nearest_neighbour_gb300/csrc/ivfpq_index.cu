@@ -435,5 +435,6 @@ extern "C" int ivfpq_add(ivfpq_index* ix, const uint8_t* codes, const int32_t* l
     ix->h_list_len[l] = h_len[l];
     ix->max_list_len = std::max<int64_t>(ix->max_list_len, h_len[l]);
   }
+  ivfpq::update_list_units(ix);
   return IVFPQ_OK;
 }

@@ -46,6 +46,7 @@ namespace ivfpq {
 constexpr int kLmWarps = 16;
 constexpr int kLmSlots = 3;  // item descriptors in flight: scanned, built, fetched
 constexpr int kLmMaxG = 8;   // queries per item at most
+constexpr int kLmMaxChunks = 16;  // chunks of one record at most
 
 struct LmParams {
   ScanParams s;                // tables, lists, codes, shapes (nprobe unused)
@@ -71,6 +72,12 @@ struct LmParams {
   uint8_t* records_w = nullptr;  // the same, for the kernels that write them
   // the kernel's i-th item is record order[i] (null: record i)
   const int32_t* order = nullptr;
+  // long lists in chunks (null: one unit of work per record): unit i is chunk
+  // units[i] % kLmMaxChunks (codes [c * unit_len, (c + 1) * unit_len)) of
+  // record units[i] / kLmMaxChunks; *n_units units
+  const int32_t* units = nullptr;
+  const int* n_units = nullptr;
+  int unit_len = 0;
   int rec_bytes;
   int dpad;                    // d rounded up to a multiple of 4
 };
@@ -217,7 +224,7 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
   const ScanParams& sp = p.s;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int jj = lane & (GS - 1), qq = lane / GS;
-  const int nit = *p.n_items;
+  const int nit = p.units ? *p.n_units : *p.n_items;
   int j = blockIdx.x;
   if (j >= nit) return;  // the same for the whole block
   const int B = gridDim.x;
@@ -237,15 +244,41 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
 
   // record of item it into slot: asynchronous copies by warp 0, completed
   // before the barrier that ends the iteration
-  auto fetch = [&](int it, int slot) {
-    if (warp != 0 || it >= nit) return;
-    const uint8_t* src = p.records + int64_t(p.order ? p.order[it] : it) * p.rec_bytes;
+  // where item it is (warp 0): its unit, its place in `order`, or it; read
+  // a step before the fetch that needs it, so the load does not stall warp 0
+  auto locate = [&](int it) {
+    if (warp != 0 || it >= nit) return 0;
+    return p.units ? p.units[it] : p.order ? p.order[it] : it;
+  };
+  // copies item it's record (record `at`, or chunk at % kLmMaxChunks of
+  // record at / kLmMaxChunks) into slot; returns the chunk, -1 if none
+  auto fetch = [&](int it, int slot, int at) {
+    if (warp != 0 || it >= nit) return -1;
+    int r = at, c = -1;
+    if (p.units) {
+      r = at / kLmMaxChunks;
+      c = at % kLmMaxChunks;
+      if (!dcheck(sp.dbg, r >= 0 && r < *p.n_items, 11)) r = 0;
+    }
+    const uint8_t* src = p.records + int64_t(r) * p.rec_bytes;
     uint8_t* dst = slots + slot * p.rec_bytes;
-    for (int c = lane; c < p.rec_bytes / 16; c += 32) lm_cp_async16(dst + 16 * c, src + 16 * c);
+    for (int q = lane; q < p.rec_bytes / 16; q += 32) lm_cp_async16(dst + 16 * q, src + 16 * q);
     asm volatile("cp.async.commit_group;" ::: "memory");
+    return c;
   };
   auto fetch_wait = [&]() {
     if (warp == 0) asm volatile("cp.async.wait_all;" ::: "memory");
+  };
+  // after fetch_wait: narrows the record in slot to chunk c of its list
+  // (warp 0, before the barrier that publishes the slot)
+  auto set_chunk = [&](int slot, int c) {
+    if (warp != 0 || c < 0) return;  // the same for the whole warp
+    __syncwarp();
+    if (lane == 0) {
+      LmHead& h = *reinterpret_cast<LmHead*>(slots + slot * p.rec_bytes);
+      h.boff += int64_t(c) * (p.unit_len / 32);
+      h.len = max(0, min(p.unit_len, h.len - c * p.unit_len));
+    }
   };
 
   // tables of the queries of the item in `slot` into half P
@@ -314,6 +347,13 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
     for (int u = 0; u < PF; ++u)
       if (warp + u * NW < nb && in_range)
         load_codes<MW>(sp.codes + (d.boff + warp + u * NW) * 32 * m, lane, cr[u]);
+  };
+  // the item's codes into L2 (its list, or the chunk of it)
+  auto prefetch = [&](int slot) {
+    const LmHead& d = head(slot);
+    const int64_t nb = (int64_t(d.len) + 31) >> 5;
+    if (nb > 0 && d.boff >= 0 && d.boff + nb <= sp.nblocks)
+      prefetch_l2(sp.codes + d.boff * 32 * m, nb * 32 * m);
   };
 
   // bound pass: this lane's TQ smallest of the current item, ascending
@@ -405,13 +445,16 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
     }
   };
 
-  fetch(j, 0);
-  fetch(j + B, 1);
+  const int c0 = fetch(j, 0, locate(j));
+  const int c1 = fetch(j + B, 1, locate(j + B));
+  int at_next = locate(j + 2 * B);
   fetch_wait();
+  set_chunk(0, c0);
+  set_chunk(1, c1);
   __syncthreads();
   build(0, 0);
   first_codes(0);
-  if (tid == 0 && j + B < nit) prefetch_list(sp, head(1).list, m);
+  if (tid == 0 && j + B < nit) prefetch(1);
   __syncthreads();
 
   int t = 0;
@@ -419,7 +462,8 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
     constexpr int P = decltype(Pc)::value;
     const int cur = t % kLmSlots, nxt = (t + 1) % kLmSlots, fil = (t + 2) % kLmSlots;
     const bool more = j + B < nit;
-    fetch(j + 2 * B, fil);
+    const int cf = fetch(j + 2 * B, fil, at_next);
+    at_next = locate(j + 3 * B);
     if (more) build(nxt, 1 - P);
     const int nqc = head(cur).nq;
     if (TQ > 0 || nqc >= G) {
@@ -446,8 +490,9 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
     }
     if (more) first_codes(nxt);
     fetch_wait();
+    set_chunk(fil, cf);
     __syncthreads();  // half P may be rebuilt next; slot fil is complete
-    if (tid == 0 && j + 2 * B < nit) prefetch_list(sp, head(fil).list, m);
+    if (tid == 0 && j + 2 * B < nit) prefetch(fil);
     j += B;
     ++t;
   };
