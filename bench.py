@@ -58,6 +58,9 @@ def parse():
     p.add_argument("--nq", type=int, default=None)
     p.add_argument("--nlist", type=int, default=None, help="list count override (development)")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--profile-range", action="store_true",
+                   help="bracket the timed searches with cudaProfilerStart/Stop (for "
+                        "ncu --profile-from-start off)")
     p.add_argument("--workload", default="large", choices=sorted(WORKLOADS),
                    help="large (default, the headline), mid, billion, flat (exact k-NN) "
                         "or kselect (stand-alone k-selection)")
@@ -354,11 +357,15 @@ def run_ours(args):
     clocks.start()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    if args.profile_range:
+        torch.cuda.profiler.start()
     ev0.record(stream)
     for _ in range(args.steps):
         B.ivfpq_search(ix, qd, NPROBE, K, out_d, out_i)
     ev1.record(stream)
     torch.cuda.synchronize()
+    if args.profile_range:
+        torch.cuda.profiler.stop()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
