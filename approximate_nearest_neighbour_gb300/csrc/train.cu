@@ -55,25 +55,38 @@ __global__ void columns_kernel(const float* __restrict__ x, int64_t n, int64_t l
 }
 
 // assignment index (int64 from the selection) -> int32 key, point index,
-// fp64 copy of the distance
+// fp64 copy of the distance; a row the selection left without a centroid (-1:
+// no finite distance, e.g. a non-finite row) gets key k, past every cluster
 __global__ void assign_prep_kernel(const int64_t* __restrict__ idx, const float* __restrict__ dist,
-                                   int64_t n, int32_t* __restrict__ key, int32_t* __restrict__ pt,
-                                   double* __restrict__ dd) {
+                                   int64_t n, int k, int32_t* __restrict__ key,
+                                   int32_t* __restrict__ pt, double* __restrict__ dd) {
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += int64_t(gridDim.x) * blockDim.x) {
-    key[i] = int32_t(idx[i]);
+    const int64_t c = idx[i];
+    key[i] = (c >= 0 && c < k) ? int32_t(c) : k;
     pt[i] = int32_t(i);
     dd[i] = double(dist[i]);
   }
 }
 
+// the final assignment: cluster, or -1 where the selection found none
+__global__ void assign_out_kernel(const int64_t* __restrict__ idx, int64_t n, int k,
+                                  int32_t* __restrict__ out) {
+  for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t c = idx[i];
+    out[i] = (c >= 0 && c < k) ? int32_t(c) : -1;
+  }
+}
+
 // [start, end) of each cluster in the sorted keys (untouched clusters stay
-// at the zero-filled [0, 0))
-__global__ void bounds_kernel(const int32_t* __restrict__ sk, int64_t n, int32_t* __restrict__ beg,
-                              int32_t* __restrict__ end) {
+// at the zero-filled [0, 0); key k, the rows without a centroid, has none)
+__global__ void bounds_kernel(const int32_t* __restrict__ sk, int64_t n, int k,
+                              int32_t* __restrict__ beg, int32_t* __restrict__ end) {
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
        i += int64_t(gridDim.x) * blockDim.x) {
     const int32_t c = sk[i];
+    if (c < 0 || c >= k) continue;
     if (i == 0 || sk[i - 1] != c) beg[c] = int32_t(i);
     if (i == n - 1 || sk[i + 1] != c) end[c] = int32_t(i + 1);
   }
@@ -97,15 +110,20 @@ __global__ void update_kernel(const float* __restrict__ x, int64_t ldx, int col0
 // codes[i][j] = argmin_e ||x_i^(j) - c_{l_i}^(j) - y_j(e)||^2 (fp32, direct
 // form, lowest e on ties); codebooks_t is [256][m][dsub4]. One thread per (i, j).
 __global__ void encode_kernel(const float* __restrict__ x, int64_t n, int d, int m, int dsub,
-                              int dsub4, const float* __restrict__ cent,
+                              int dsub4, const float* __restrict__ cent, int nlist,
                               const int32_t* __restrict__ lists,
                               const float* __restrict__ cb_t, uint8_t* __restrict__ codes) {
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n * m;
        i += int64_t(gridDim.x) * blockDim.x) {
     const int64_t r = i / m;
     const int j = int(i - r * m);
+    const int l = lists[r];
+    if (l < 0 || l >= nlist) {  // no centroid (a non-finite row): code 0
+      codes[i] = 0;
+      continue;
+    }
     const float* xr = x + r * d + j * dsub;
-    const float* cr = cent + int64_t(lists[r]) * d + j * dsub;
+    const float* cr = cent + int64_t(l) * d + j * dsub;
     float res[32];
     for (int t = 0; t < dsub; ++t) res[t] = xr[t] - cr[t];
     float best = INFINITY;
@@ -128,12 +146,14 @@ __global__ void encode_kernel(const float* __restrict__ x, int64_t n, int d, int
 
 // r[i] = x[i] - c[lists[i]] (rows of d floats)
 __global__ void residual_kernel(const float* __restrict__ x, int64_t n, int d,
-                                const float* __restrict__ cent, const int32_t* __restrict__ lists,
-                                float* __restrict__ r) {
+                                const float* __restrict__ cent, int nlist,
+                                const int32_t* __restrict__ lists, float* __restrict__ r) {
   for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < n * d;
        i += int64_t(gridDim.x) * blockDim.x) {
     const int64_t row = i / d;
-    r[i] = x[i] - cent[int64_t(lists[row]) * d + int(i - row * d)];
+    const int l = lists[row];
+    // no centroid (list -1: a non-finite row): NaN residual
+    r[i] = (l >= 0 && l < nlist) ? x[i] - cent[int64_t(l) * d + int(i - row * d)] : NAN;
   }
 }
 
@@ -244,8 +264,8 @@ int lloyd(const float* y, int64_t n, int d, int k, int niter, float* c, int32_t*
   IVFPQ_TRY(ws.alloc(&end, size_t(k)));
   IVFPQ_TRY(ws.alloc(&dd, size_t(n)));
   IVFPQ_TRY(ws.alloc(&dsum, 1));
-  int end_bit = 1;
-  while ((int64_t(1) << end_bit) < k) ++end_bit;
+  int end_bit = 1;  // keys 0 .. k (k: no centroid)
+  while ((int64_t(1) << end_bit) < int64_t(k) + 1) ++end_bit;
   size_t sort_bytes = 0, red_bytes = 0;
   IVFPQ_CUDA(cub::DeviceRadixSort::SortPairs(nullptr, sort_bytes, key, skey, pt, spt, n, 0,
                                              end_bit, s));
@@ -259,7 +279,7 @@ int lloyd(const float* y, int64_t n, int d, int k, int niter, float* c, int32_t*
   o.idx64 = idx;
   for (int it = 0; it <= niter; ++it) {
     IVFPQ_TRY(knn_by_tiles(y, n, c, k, d, 1, o, s));
-    assign_prep_kernel<<<grid1(n, 256), 256, 0, s>>>(idx, dist, n, key, pt, dd);
+    assign_prep_kernel<<<grid1(n, 256), 256, 0, s>>>(idx, dist, n, k, key, pt, dd);
     IVFPQ_LAUNCHED();
     if (obj) {
       IVFPQ_CUDA(cub::DeviceReduce::Sum(red_tmp, red_bytes, dd, dsum, n, s));
@@ -267,16 +287,17 @@ int lloyd(const float* y, int64_t n, int d, int k, int niter, float* c, int32_t*
       IVFPQ_CUDA(cudaStreamSynchronize(s));
     }
     if (it == niter) {
-      if (assign_out)
-        IVFPQ_CUDA(cudaMemcpyAsync(assign_out, key, size_t(n) * sizeof(int32_t),
-                                   cudaMemcpyDeviceToDevice, s));
+      if (assign_out) {
+        assign_out_kernel<<<grid1(n, 256), 256, 0, s>>>(idx, n, k, assign_out);
+        IVFPQ_LAUNCHED();
+      }
       break;
     }
     IVFPQ_CUDA(cub::DeviceRadixSort::SortPairs(sort_tmp, sort_bytes, key, skey, pt, spt, n, 0,
                                                end_bit, s));
     IVFPQ_CUDA(cudaMemsetAsync(beg, 0, size_t(k) * sizeof(int32_t), s));
     IVFPQ_CUDA(cudaMemsetAsync(end, 0, size_t(k) * sizeof(int32_t), s));
-    bounds_kernel<<<grid1(n, 256), 256, 0, s>>>(skey, n, beg, end);
+    bounds_kernel<<<grid1(n, 256), 256, 0, s>>>(skey, n, k, beg, end);
     IVFPQ_LAUNCHED();
     update_kernel<<<unsigned(k), 128, 0, s>>>(y, d, 0, d, spt, beg, end, c);
     IVFPQ_LAUNCHED();
@@ -368,8 +389,8 @@ extern "C" int ivfpq_encode(const ivfpq_index* ix, const float* x, int64_t n, in
   IVFPQ_TRY(knn_by_tiles(x, n, ix->centroids, ix->nlist, ix->d, 1, o, s,
                          ix->cent_hi ? &xo : nullptr));
   encode_kernel<<<grid1(n * ix->m, 256), 256, 0, s>>>(x, n, ix->d, ix->m, ix->dsub, ix->dsub4,
-                                                      ix->centroids, list_ids, ix->codebooks,
-                                                      codes);
+                                                      ix->centroids, ix->nlist, list_ids,
+                                                      ix->codebooks, codes);
   IVFPQ_LAUNCHED();
   return IVFPQ_OK;
 }
@@ -442,7 +463,8 @@ extern "C" int ivfpq_residuals(const float* centroids, int nlist, int d, const f
   o.kind = OutKind::Probes;
   o.idx32 = list_ids;
   IVFPQ_TRY(knn_by_tiles(x, n, centroids, nlist, d, 1, o, s));
-  residual_kernel<<<grid1(n * d, 256), 256, 0, s>>>(x, n, d, centroids, list_ids, residuals);
+  residual_kernel<<<grid1(n * d, 256), 256, 0, s>>>(x, n, d, centroids, nlist, list_ids,
+                                                   residuals);
   IVFPQ_LAUNCHED();
   return IVFPQ_OK;
 }
@@ -500,8 +522,8 @@ extern "C" int ivfpq_encode_hinted(const ivfpq_index* ix, const float* x, int64_
     IVFPQ_LAUNCHED();
   }
   encode_kernel<<<grid1(n * ix->m, 256), 256, 0, s>>>(x, n, ix->d, ix->m, ix->dsub, ix->dsub4,
-                                                      ix->centroids, list_ids, ix->codebooks,
-                                                      codes);
+                                                      ix->centroids, ix->nlist, list_ids,
+                                                      ix->codebooks, codes);
   IVFPQ_LAUNCHED();
   if (n_searched) *n_searched = cnt;
   return IVFPQ_OK;

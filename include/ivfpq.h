@@ -314,6 +314,10 @@ int ivfpq_knn_graph(const ivfpq_index* index, const float* x, const int64_t* sel
  *  niter      number of updates (>= 0); niter + 1 assignment passes
  *  centroids  device fp32 [k, d] (out)
  *  assign     device int32 [n] (out, may be NULL): the final assignment
+ * A row holding NaN has no finite distance: the search may leave it without a
+ * centroid (assignment -1, the row joins no cluster) or assign it at distance
+ * NaN (its cluster's mean and the objective become NaN); either way nothing
+ * outside the arguments is read or written.
  *  objective  HOST fp64 [niter + 1] (out, may be NULL): sum of squared
  *             distances to the assigned centroid at each assignment pass
  * The update is the mean of each cluster's points summed in fp64 in
@@ -346,9 +350,12 @@ int pq_train(const float* x, int64_t n, int d, int m, int niter, const int64_t* 
  * Source: "Custom 8-bit floating point value format ...", index construction
  * steps 1-3 (nearest centroid, residual, nearest codeword per sub-space).
  *  x         device fp32 [n, index d]
- *  list_ids  device int32 [n] (out): nearest centroid (exact distances)
+ *  list_ids  device int32 [n] (out): nearest centroid (exact distances); a
+ *            row holding NaN may get -1 (no finite distance to any centroid),
+ *            which ivfpq_add rejects
  *  codes     device uint8 [n, m] (out): per sub-space, the codeword nearest
- *            to the residual's sub-vector (fp32 distances, lowest index on ties)
+ *            to the residual's sub-vector (fp32 distances, lowest index on
+ *            ties); zeros for a row with list -1
  * Asynchronous. Errors: INVALID_ARG (also d/m > 32), OOM, CUDA.
  */
 int ivfpq_encode(const ivfpq_index* index, const float* x, int64_t n, int32_t* list_ids,
@@ -363,8 +370,10 @@ int ivfpq_encode(const ivfpq_index* index, const float* x, int64_t n, int32_t* l
  * search with GPUs", section 5 (the product quantizer encodes residuals).
  *  centroids  device fp32 [nlist, d];  x  device fp32 [n, d], n < 2^31
  *  list_ids   device int32 [n] (out): nearest centroid (exact distances;
- *             equal distances go to either centroid)
- *  residuals  device fp32 [n, d] (out): x - centroids[list_ids]
+ *             equal distances go to either centroid); a row holding NaN
+ *             may get -1 (no finite distance to any centroid)
+ *  residuals  device fp32 [n, d] (out): x - centroids[list_ids]; NaN for a
+ *             row with list -1
  * Asynchronous. Errors: INVALID_ARG, OOM, CUDA.
  */
 int ivfpq_residuals(const float* centroids, int nlist, int d, const float* x, int64_t n,

@@ -135,3 +135,38 @@ def test_index_built_from_raw_vectors_follows_the_oracle(B):
     od, oi, _ = oracle.ivfpq_search(q, wi.cent, cb, off, codes_l, ids_l, 16, 164,
                                     forced_probes=gp)
     compare_knn(gd.cpu().numpy(), gi.cpu().numpy(), od, oi, context="built index")
+
+
+def test_rows_holding_nan_touch_nothing_outside_the_arguments(B):
+    """A row holding NaN has no finite distance to any centroid. With 4,096
+    centroids the coarse search takes the filtered plan, which keeps no
+    candidate for such a row: its list is -1, its residual NaN and its codes
+    zero, and ivfpq_add refuses it; the finite rows are unaffected."""
+    import torch
+    nlist, d, m = 4096, 32, 8
+    cent, _, x = _mixture(6, nlist, d, 3000)
+    bad = np.array([5, 77, 2999])
+    x[bad] = np.nan
+    good = np.setdiff1d(np.arange(3000), bad)
+    lists, resid = B.ivfpq_residuals(_t(cent), _t(x))
+    torch.cuda.synchronize()
+    lists, resid = lists.cpu().numpy(), resid.cpu().numpy()
+    assert np.all((lists[bad] >= -1) & (lists[bad] < nlist))
+    assert np.all(np.isnan(resid[bad]))
+    ol, od = oracle.coarse(x[good], cent, 1)
+    for i, r in enumerate(good):
+        if lists[r] != ol[i, 0]:
+            dr = ((x[r].astype(np.float64) - cent[lists[r]]) ** 2).sum()
+            assert dr - od[i, 0] <= 1e-5 * max(od[i, 0], 1e-6), r
+    assert np.array_equal(resid[good], x[good] - cent[lists[good]])
+    cb = (0.15 * np.random.default_rng(7).standard_normal((m, 256, d // m))).astype(np.float32)
+    ix = B.ivfpq_index_create(_t(cent), _t(cb))
+    el, ec = B.ivfpq_encode(ix, _t(x))
+    torch.cuda.synchronize()
+    el, ec = el.cpu().numpy(), ec.cpu().numpy()
+    assert np.array_equal(el[good], lists[good])
+    assert np.all(ec[bad][el[bad] == -1] == 0)
+    _check_codes(x[good], el[good], ec[good], cent, cb, "finite rows")
+    if np.any(el == -1):
+        with pytest.raises(B.IVFPQError):
+            B.ivfpq_add(ix, _t(ec), _t(el), _t(np.arange(3000, dtype=np.int64)))
