@@ -167,26 +167,30 @@ namespace {
 
 // Long rows: one block of 16 warps per row.
 //  1. A bound: a 4096-bin histogram of the top 12 key bits of the row's first
-//     `sample` values (sample >= k). The bin holding the sample's k-th
-//     smallest key ends at theta; at least k values of the row are <= theta,
-//     so every value of the row's k smallest is <= theta as well.
+//     `sample` values (sample >= k) finds the bin holding the sample's k-th
+//     smallest key; a second histogram, of the next 12 bits of the sample
+//     keys in that bin, narrows it to a sub-bin of 256 keys, whose end is
+//     theta. At least k values of the row are <= theta (the sample's k
+//     smallest), so every value of the row's k smallest is <= theta as well,
+//     and about k * cols / sample values pass.
 //  2. The warps stream the row (thread t of the block takes float4 t, t + 512,
 //     ... when the row is 16-byte aligned, single floats otherwise) and append
 //     every key <= theta with its column to a shared buffer of `cap` entries
-//     (one atomic per warp and value position).
+//     (per float4: a warp scan of the lanes' passing counts and one atomic per
+//     warp).
 //  3. One bitonic sort of the buffer; its first k entries are the result.
 // There are at least k candidates (the sample's own). A row with more than
 // `cap` writes nothing and sets flags[row] = 1 for the full-queue kernel.
 __global__ void __launch_bounds__(512)
 row_cand_kernel(const float* __restrict__ vals, int64_t cols, int64_t sample, int k, int cap,
                 OutWriter out, int* __restrict__ flags) {
-  constexpr int kBins = 4096, kShift = 20, kPer = kBins / 512;
+  constexpr int kBins = 4096, kShift = 20, kSub = 8, kPer = kBins / 512;
   extern __shared__ uint32_t sm_cand[];
   uint32_t* hist = sm_cand;
   uint32_t* ck = sm_cand + kBins;
   uint32_t* ci = ck + cap;
   __shared__ uint32_t part[16];
-  __shared__ uint32_t theta_s, count_s;
+  __shared__ uint32_t theta_s, count_s, bin_s, need_s;
   const int64_t row = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* rp = vals + row * cols;
@@ -194,6 +198,8 @@ row_cand_kernel(const float* __restrict__ vals, int64_t cols, int64_t sample, in
   if (threadIdx.x == 0) {
     theta_s = kSentinelKey;
     count_s = 0;
+    bin_s = kBins - 1;
+    need_s = 0;
   }
   __syncthreads();
   for (int64_t c = threadIdx.x; c < sample; c += 512)
@@ -221,10 +227,52 @@ row_cand_kernel(const float* __restrict__ vals, int64_t cols, int64_t sample, in
     if (run < uint32_t(k) && run + sum >= uint32_t(k)) {
 #pragma unroll
       for (int i = 0; i < kPer; ++i) {
+        if (run + h[i] >= uint32_t(k)) {
+          bin_s = threadIdx.x * kPer + i;
+          need_s = uint32_t(k) - run;  // of the bin's sample keys, in order
+          break;
+        }
         run += h[i];
-        if (run >= uint32_t(k)) {
-          const uint32_t b = threadIdx.x * kPer + i;
-          theta_s = b == kBins - 1 ? kSentinelKey : ((b + 1) << kShift) - 1;
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t bin = bin_s;
+  if (bin == kBins - 1) {  // the top bin (NaN keys and the sentinel's): no bound
+    if (threadIdx.x == 0) theta_s = kSentinelKey;
+  } else {
+    // the next 12 key bits of the sample keys in that bin
+    for (int b = threadIdx.x; b < kBins; b += 512) hist[b] = 0;
+    __syncthreads();
+    for (int64_t c = threadIdx.x; c < sample; c += 512) {
+      const uint32_t key = float_to_key(__ldg(rp + c));
+      if ((key >> kShift) == bin) atomicAdd(&hist[(key >> kSub) & (kBins - 1)], 1u);
+    }
+    __syncthreads();
+    uint32_t h[kPer], sum = 0;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      h[i] = hist[threadIdx.x * kPer + i];
+      sum += h[i];
+    }
+    uint32_t inc = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o *= 2) {
+      const uint32_t v = __shfl_up_sync(kFullMask, inc, o);
+      if (lane >= o) inc += v;
+    }
+    if (lane == 31) part[warp] = inc;
+    __syncthreads();
+    uint32_t run = inc - sum;
+    for (int w = 0; w < warp; ++w) run += part[w];
+    const uint32_t need = need_s;
+    if (run < need && run + sum >= need) {
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        run += h[i];
+        if (run >= need) {
+          const uint32_t sb = threadIdx.x * kPer + i;
+          theta_s = (bin << kShift) | (sb << kSub) | ((1u << kSub) - 1u);
           break;
         }
       }
@@ -270,13 +318,35 @@ row_cand_kernel(const float* __restrict__ vals, int64_t cols, int64_t sample, in
       const uint32_t k1 = ok ? float_to_key(x.y) : kSentinelKey;
       const uint32_t k2 = ok ? float_to_key(x.z) : kSentinelKey;
       const uint32_t k3 = ok ? float_to_key(x.w) : kSentinelKey;
-      const uint32_t lo = min(min(k0, k1), min(k2, k3));
-      if (__any_sync(kFullMask, ok && lo <= theta)) {
+      const uint32_t pm = ok ? uint32_t(k0 <= theta) | (uint32_t(k1 <= theta) << 1) |
+                                   (uint32_t(k2 <= theta) << 2) | (uint32_t(k3 <= theta) << 3)
+                             : 0u;
+      if (__any_sync(kFullMask, pm != 0u)) {
+        // this lane's passing keys go to consecutive slots after those of
+        // the lanes below it: an inclusive warp scan of the counts, one
+        // atomic for the warp's total
+        const uint32_t cnt = __popc(pm);
+        uint32_t inc = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o *= 2) {
+          const uint32_t v = __shfl_up_sync(kFullMask, inc, o);
+          if (lane >= o) inc += v;
+        }
+        uint32_t base = 0;
+        if (lane == 31) base = atomicAdd(&count_s, inc);
+        uint32_t pos = __shfl_sync(kFullMask, base, 31) + inc - cnt;
         const uint32_t c = uint32_t(i4 * 4);
-        append(ok && k0 <= theta, k0, c);
-        append(ok && k1 <= theta, k1, c + 1);
-        append(ok && k2 <= theta, k2, c + 2);
-        append(ok && k3 <= theta, k3, c + 3);
+        const uint32_t kk[4] = {k0, k1, k2, k3};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if ((pm >> j) & 1u) {
+            if (pos < uint32_t(cap)) {
+              ck[pos] = kk[j];
+              ci[pos] = c + j;
+            }
+            ++pos;
+          }
+        }
       }
     }
   } else {
@@ -328,7 +398,7 @@ row_cand_kernel(const float* __restrict__ vals, int64_t cols, int64_t sample, in
 int select_rows_cand(const float* vals, int64_t rows, int64_t cols, int k, const SelectOut& out,
                      cudaStream_t s) {
   constexpr int kMaxCap = 16384;
-  const int64_t sample = std::min<int64_t>(cols / 2, std::max<int64_t>(8192, 32 * int64_t(k)));
+  const int64_t sample = std::min<int64_t>(cols / 2, std::max<int64_t>(16384, 32 * int64_t(k)));
   const int64_t expect = ceil_div(int64_t(k) * cols, sample);
   int cap = 1024;
   while (cap < 2 * expect + 512 && cap < kMaxCap) cap *= 2;

@@ -65,6 +65,8 @@ def parse():
                    help="large (default, the headline), mid, billion, flat (exact k-NN) "
                         "or kselect (stand-alone k-selection)")
     p.add_argument("--k", type=int, default=None, help="k override")
+    p.add_argument("--nprobe", type=int, default=None,
+                   help="nprobe override (IVF-PQ workloads; the mid workload states 16 and 64)")
     p.add_argument("--scan-mode", type=int, default=-1, choices=[-1, 0, 1],
                    help="list scan organisation: -1 automatic, 0 by query, 1 by list")
     return p.parse_args()
@@ -423,7 +425,8 @@ def run_ours(args):
         lookup_peak = nsm * LOOKUPS_PER_SM_CLOCK * per_word * sm_mhz * 1e6
         lookups_per_s = scan_bytes / (scan_ms / 1e3)
         if traffic is not None and (args.n is not None or args.nlist is not None
-                                    or args.workload != "large"):
+                                    or args.workload != "large" or args.lut != "fp32"
+                                    or args.nprobe is not None or args.k is not None):
             traffic = None
         total_q = nq * world * args.steps
         line = {
@@ -729,6 +732,8 @@ def main():
         args.lut = "fp16" if args.workload == "billion" else "fp32"
     if args.k is not None:
         K = args.k
+    if args.nprobe is not None:
+        NPROBE = args.nprobe
     if args.workload == "kselect":
         run_kselect(args)
     elif args.workload == "flat":
