@@ -46,6 +46,19 @@ int select_rows(const float* vals, int64_t rows, int64_t cols, int k, int64_t ch
 int select_pairs(const uint32_t* keys, const uint32_t* idx, int64_t rows, int64_t len, int k,
                  int64_t chunks, int64_t chunk_len, const SelectOut& out, cudaStream_t s);
 
+// Radix-bound selection, one block per row (select_radix.cu).
+// bound[r] = a float >= the k-th smallest of row r of vals (+inf if none).
+int row_kth_bound(const float* vals, int64_t rows, int64_t cols, int k, float* bound,
+                  cudaStream_t s);
+// The k smallest entries of each row's candidate segments (as
+// select_candidates), sorted; flags[r] = 1 where row r was not written (an
+// overflowed segment, or too many entries tie around the bound), else 0.
+int cand_radix_select(const uint64_t* cand, const int* scnt, int nseg, int cap_s, int64_t rows,
+                      int k, const SelectOut& out, int* flags, cudaStream_t s);
+// Each row's len (key, index) pairs sorted, the first k written (len <= 8192).
+int sort_pairs_rows(const uint32_t* keys, const uint32_t* idx, int64_t rows, int len, int k,
+                    const SelectOut& out, cudaStream_t s);
+
 // The k smallest of each row's `runs` runs of kw (key, index) pairs, each run
 // sorted ascending (rows of runs * kw entries): a bitonic merge tree in shared
 // memory (the pair selection when runs * kw exceeds 8,192).

@@ -71,74 +71,6 @@ cand_select_kernel(const uint64_t* __restrict__ cand, const int* __restrict__ sc
   }
 }
 
-// Long queues (k > 256), first level: 16 warps per row, each keeping the KW
-// best of its segments (g = warp mod 16) and writing them unmerged to
-// pk/pi[row][warp][KW]. A row with an overflowed segment gets over[row] = 1
-// and sentinels (it is selected again by the block kernel).
-template <int KW>
-__global__ void __launch_bounds__(512)
-cand_short_kernel(const uint64_t* __restrict__ cand, const int* __restrict__ scnt, int nseg,
-                  int cap_s, uint32_t* __restrict__ pk, uint32_t* __restrict__ pi,
-                  int* __restrict__ over_out) {
-  constexpr int T = ThreadQ<KW>::value;
-  const int64_t row = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int* cnt = scnt + row * nseg;
-  int over = 0;
-  for (int g = threadIdx.x; g < nseg; g += 512) over |= cnt[g] > cap_s;
-  over = __syncthreads_or(over);
-  WarpSelect<KW, T> ws;
-  ws.init(lane);
-  if (!over) {
-    for (int g = warp; g < nseg; g += 16) {
-      const int ns = max(cnt[g], 0);
-      const uint64_t* e = cand + (row * nseg + g) * cap_s;
-      for (int base = 0; base < ns; base += 32) {
-        const int i = base + lane;
-        const bool ok = i < ns;
-        const uint64_t v = ok ? __ldcs(e + i) : ~uint64_t(0);
-        ws.add(uint32_t(v >> 32), uint32_t(v));
-      }
-    }
-    ws.finalize();
-  }
-  const int64_t o = (row * 16 + warp) * KW;
-#pragma unroll
-  for (int r = 0; r < KW / 32; ++r) {
-    pk[o + 32 * r + lane] = ws.wk[r];
-    pi[o + 32 * r + lane] = ws.wv[r];
-  }
-  if (threadIdx.x == 0) over_out[row] = over;
-}
-
-// flags[row] = 1 if the merged k best (tk, ascending, [rows][k]) may miss an
-// entry a full warp queue dropped (its last key not above the k-th), or the
-// row overflowed.
-template <int KW>
-__global__ void cand_short_check_kernel(const uint32_t* __restrict__ pk, const uint32_t* __restrict__ tk,
-                                        const int* __restrict__ over, int64_t rows, int k,
-                                        int* __restrict__ flags) {
-  const int64_t r = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (r >= rows) return;
-  const uint32_t theta = tk[r * k + k - 1];
-  int f = over[r];
-  for (int w = 0; w < 16; ++w) {
-    const uint32_t last = pk[(r * 16 + w) * KW + KW - 1];
-    f |= last != kSentinelKey && last <= theta;
-  }
-  flags[r] = f;
-}
-
-// Writes the ascending (key, index) rows [rows][k] through the output writer.
-static __global__ void cand_emit_kernel(const uint32_t* __restrict__ tk, const uint32_t* __restrict__ ti,
-                                 int64_t rows, int k, OutWriter out) {
-  for (int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; t < rows * k;
-       t += int64_t(gridDim.x) * blockDim.x) {
-    const int64_t r = t / k;
-    out.write(r, 0, int(t - r * k), tk[t], ti[t]);
-  }
-}
-
 // One warp per row (4 rows per block), for queue lengths up to 256: no
 // block-level merge.
 template <int K>
@@ -210,31 +142,9 @@ int launch_cand(const uint64_t* cand, const int* scnt, int nseg, int cap_s, int6
   return IVFPQ_OK;
 }
 
-template <int KW>
-int launch_cand_short(const uint64_t* cand, const int* scnt, int nseg, int cap_s, int64_t rows,
-                      uint32_t* pk, uint32_t* pi, int* over, cudaStream_t s) {
-  auto kern = cand_short_kernel<KW>;
-  kern<<<unsigned(rows), 512, 0, s>>>(cand, scnt, nseg, cap_s, pk, pi, over);
-  IVFPQ_LAUNCHED_K(kern, 0, 512);
-  return IVFPQ_OK;
-}
-
-template <int KW>
-int launch_cand_check(const uint32_t* pk, const uint32_t* tk, const int* over, int64_t rows,
-                      int k, int* flags, cudaStream_t s) {
-  cand_short_check_kernel<KW><<<unsigned(ceil_div(rows, 256)), 256, 0, s>>>(pk, tk, over, rows, k,
-                                                                           flags);
-  IVFPQ_LAUNCHED();
-  return IVFPQ_OK;
-}
-
 }  // namespace ivfpq
 
 #define IVFPQ_INST_CAND(K)                                                                   \
   template int ivfpq::launch_cand<K>(const uint64_t*, const int*, int, int, int64_t,         \
                                      const float*, const float*, int64_t, int,               \
-                                     const ivfpq::OutWriter&, cudaStream_t);                  \
-  template int ivfpq::launch_cand_short<K / 8>(const uint64_t*, const int*, int, int, int64_t, \
-                                               uint32_t*, uint32_t*, int*, cudaStream_t);   \
-  template int ivfpq::launch_cand_check<K / 8>(const uint32_t*, const uint32_t*, const int*,  \
-                                               int64_t, int, int*, cudaStream_t);
+                                     const ivfpq::OutWriter&, cudaStream_t);

@@ -59,7 +59,7 @@ def parse():
     p.add_argument("--nlist", type=int, default=None, help="list count override (development)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--profile-range", action="store_true",
-                   help="bracket the timed searches with cudaProfilerStart/Stop (for "
+                   help="bracket the timed calls with cudaProfilerStart/Stop (for "
                         "ncu --profile-from-start off)")
     p.add_argument("--workload", default="large", choices=sorted(WORKLOADS),
                    help="large (default, the headline), mid, billion, flat (exact k-NN) "
@@ -518,11 +518,15 @@ def run_flat(args):
     clocks.start()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
+    if args.profile_range:
+        torch.cuda.profiler.start()
     ev0.record(stream)
     for _ in range(args.steps):
         B.flat_knn(dbd, qd, K, out_d, out_i)
     ev1.record(stream)
     torch.cuda.synchronize()
+    if args.profile_range:
+        torch.cuda.profiler.stop()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
@@ -643,11 +647,15 @@ def run_kselect(args):
     clocks.start()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    if args.profile_range:
+        torch.cuda.profiler.start()
     e0.record(stream)
     for _ in range(args.steps):
         B.kselect(vals, K, out_v, out_i)
     e1.record(stream)
     torch.cuda.synchronize()
+    if args.profile_range:
+        torch.cuda.profiler.stop()
     clk = clocks.stop()
     launches = B.kernel_launches() - launches0
     call_s = e0.elapsed_time(e1) / 1e3 / args.steps

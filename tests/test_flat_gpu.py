@@ -110,3 +110,23 @@ def test_expired_wait_is_reported_and_the_context_stays_usable(B):
     od, oi = oracle.flat_knn(db, q, 5 + 64)
     compare_knn(gd, gi, od, oi, context="after timeout")
     B.device_check()
+
+
+@pytest.mark.parametrize("k", [300, 1024])
+def test_flat_ties_beyond_the_selection_buffer(B, k):
+    """2,000 copies of one vector sit next to every query, spread over the
+    database: the k nearest all tie, more entries than the radix selection's
+    buffer fall under its bound, and those rows are selected again by the
+    full-length kernel. Any k of the copies is a valid answer."""
+    rng = np.random.default_rng(k)
+    n, d, nq = 30_000, 32, 64
+    db = 3 * rng.standard_normal((n, d)).astype(np.float32)
+    v = rng.standard_normal(d).astype(np.float32)
+    db[::15] = v
+    q = (v + 0.01 * rng.standard_normal((nq, d))).astype(np.float32)
+    gd, gi = _flat(B, db, q, k)
+    od, oi = oracle.flat_knn(db, q, 2000 + 64)  # every tied copy is a valid answer
+    compare_knn(gd, gi, od, oi, context="flat ties")
+    copies = set(range(0, n, 15))
+    for r in range(nq):
+        assert len(set(gi[r].tolist())) == k and set(gi[r].tolist()) <= copies
