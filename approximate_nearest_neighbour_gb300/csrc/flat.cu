@@ -42,6 +42,39 @@ __global__ void rerank_kernel(const float* __restrict__ Q, const float* __restri
     cols[w] = uint32_t(c);
   }
 }
+// The same with float4 loads (d a multiple of 4, 16-byte aligned rows): 8
+// lanes per entry, 4 entries per warp, each lane up to d / 32 float4 of the
+// query and of the database row in flight.
+__global__ void rerank4_kernel(const float* __restrict__ Q, const float* __restrict__ X, int d,
+                               int64_t rows, int k, const int64_t* __restrict__ idx64,
+                               const int32_t* __restrict__ idx32, uint32_t* __restrict__ keys,
+                               uint32_t* __restrict__ cols) {
+  const int64_t e = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 3;
+  const int sub = threadIdx.x & 7;
+  const bool live = e < rows * k;  // lanes past the end stay for the shuffles
+  const int64_t r = live ? e / k : 0;
+  const int64_t c = live ? (idx64 ? idx64[e] : int64_t(idx32[e])) : -1;
+  float s = 0.f;
+  if (c >= 0) {
+    const float4* q4 = reinterpret_cast<const float4*>(Q + r * d);
+    const float4* x4 = reinterpret_cast<const float4*>(X + c * d);
+    for (int j = sub; j < d / 4; j += 8) {
+      const float4 a = __ldg(q4 + j), b = __ldg(x4 + j);
+      const float dx = a.x - b.x, dy = a.y - b.y, dz = a.z - b.z, dw = a.w - b.w;
+      s = fmaf(dx, dx, s);
+      s = fmaf(dy, dy, s);
+      s = fmaf(dz, dz, s);
+      s = fmaf(dw, dw, s);
+    }
+  }
+  s += __shfl_xor_sync(kFullMask, s, 4);
+  s += __shfl_xor_sync(kFullMask, s, 2);
+  s += __shfl_xor_sync(kFullMask, s, 1);
+  if (live && sub == 0) {
+    keys[e] = c < 0 ? kSentinelKey : float_to_key(s);
+    cols[e] = c < 0 ? kSentinelIdx : uint32_t(c);
+  }
+}
 }  // namespace
 
 // Bytes of distance workspace per query tile.
@@ -57,8 +90,15 @@ int rerank(const float* Q, const float* X, int d, int64_t rows, int k, const Sel
   uint32_t* rk = scratch;
   uint32_t* rc = rk + rows * k;
   const int64_t warps = rows * k;
-  rerank_kernel<<<unsigned(ceil_div(warps * 32, 256)), 256, 0, s>>>(
-      Q, X, d, rows, k, o.idx64, o.kind == OutKind::Probes ? o.idx32 : nullptr, rk, rc);
+  const bool vec = d % 4 == 0 && (reinterpret_cast<uintptr_t>(Q) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(X) & 15) == 0;
+  if (vec) {
+    rerank4_kernel<<<unsigned(ceil_div(warps * 8, 256)), 256, 0, s>>>(
+        Q, X, d, rows, k, o.idx64, o.kind == OutKind::Probes ? o.idx32 : nullptr, rk, rc);
+  } else {
+    rerank_kernel<<<unsigned(ceil_div(warps * 32, 256)), 256, 0, s>>>(
+        Q, X, d, rows, k, o.idx64, o.kind == OutKind::Probes ? o.idx32 : nullptr, rk, rc);
+  }
   IVFPQ_LAUNCHED();
   // k > 256: one bitonic sort per row (the pair selection's k-entry queues
   // took 1.8 ms of a 10,000-query flat k = 1024 call)
