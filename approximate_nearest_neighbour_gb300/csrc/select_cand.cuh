@@ -81,7 +81,8 @@ cand_select_warp_kernel(const uint64_t* __restrict__ cand, const int* __restrict
   constexpr int T = ThreadQ<K>::value;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = int64_t(blockIdx.x) * 4 + warp;
-  if (row >= rows) return;  // the whole warp
+  if (row >= rows) return;                               // the whole warp
+  if (out.o.row_mask && !out.o.row_mask[row]) return;  // the whole warp
   const int* cnt = scnt + row * nseg;
   int over = 0;
   for (int g = lane; g < nseg; g += 32) over |= cnt[g] > cap_s;
