@@ -181,7 +181,7 @@ namespace {
 //  3. One bitonic sort of the buffer; its first k entries are the result.
 // There are at least k candidates (the sample's own). A row with more than
 // `cap` writes nothing and sets flags[row] = 1 for the full-queue kernel.
-__global__ void __launch_bounds__(512)
+__global__ void __launch_bounds__(512, 3)
 row_cand_kernel(const float* __restrict__ vals, int64_t cols, int64_t sample, int k, int cap,
                 OutWriter out, int* __restrict__ flags) {
   constexpr int kBins = 4096, kShift = 20, kSub = 8, kPer = kBins / 512;
@@ -297,54 +297,54 @@ row_cand_kernel(const float* __restrict__ vals, int64_t cols, int64_t sample, in
   };
   const bool vec = (cols & 3) == 0 && (reinterpret_cast<uintptr_t>(vals) & 15) == 0;
   if (vec) {
-    // four float4 loads in flight per thread (a rotating buffer); one vote
-    // per float4 skips the appends when no lane holds a key <= theta
+    // four float4 loads in flight per thread (a ring of four, unrolled so
+    // that no register moves between slots); one vote per float4 skips the
+    // appends when no lane holds a key <= theta
     const float4* p4 = reinterpret_cast<const float4*>(rp);
     const int64_t n4 = cols >> 2;
     auto ld = [&](int64_t i4) {
       return i4 < n4 ? __ldcs(p4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
     };
-    float4 b0 = ld(threadIdx.x), b1 = ld(threadIdx.x + 512), b2 = ld(threadIdx.x + 1024),
-           b3 = ld(threadIdx.x + 1536);
+    float4 ring[4] = {ld(threadIdx.x), ld(threadIdx.x + 512), ld(threadIdx.x + 1024),
+                      ld(threadIdx.x + 1536)};
 #pragma unroll 1
-    for (int64_t i4 = threadIdx.x; i4 - threadIdx.x < n4; i4 += 512) {
-      const float4 x = b0;
-      b0 = b1;
-      b1 = b2;
-      b2 = b3;
-      b3 = ld(i4 + 2048);
-      const bool ok = i4 < n4;
-      const uint32_t k0 = ok ? float_to_key(x.x) : kSentinelKey;
-      const uint32_t k1 = ok ? float_to_key(x.y) : kSentinelKey;
-      const uint32_t k2 = ok ? float_to_key(x.z) : kSentinelKey;
-      const uint32_t k3 = ok ? float_to_key(x.w) : kSentinelKey;
-      const uint32_t pm = ok ? uint32_t(k0 <= theta) | (uint32_t(k1 <= theta) << 1) |
-                                   (uint32_t(k2 <= theta) << 2) | (uint32_t(k3 <= theta) << 3)
-                             : 0u;
-      if (__any_sync(kFullMask, pm != 0u)) {
-        // this lane's passing keys go to consecutive slots after those of
-        // the lanes below it: an inclusive warp scan of the counts, one
-        // atomic for the warp's total
-        const uint32_t cnt = __popc(pm);
-        uint32_t inc = cnt;
+    for (int64_t base = threadIdx.x; base - threadIdx.x < n4; base += 2048) {
 #pragma unroll
-        for (int o = 1; o < 32; o *= 2) {
-          const uint32_t v = __shfl_up_sync(kFullMask, inc, o);
-          if (lane >= o) inc += v;
-        }
-        uint32_t base = 0;
-        if (lane == 31) base = atomicAdd(&count_s, inc);
-        uint32_t pos = __shfl_sync(kFullMask, base, 31) + inc - cnt;
-        const uint32_t c = uint32_t(i4 * 4);
-        const uint32_t kk[4] = {k0, k1, k2, k3};
+      for (int u = 0; u < 4; ++u) {
+        const int64_t i4 = base + 512 * u;
+        const float4 x = ring[u];
+        ring[u] = ld(i4 + 2048);
+        const bool ok = i4 < n4;
+        const uint32_t k0 = float_to_key(x.x), k1 = float_to_key(x.y);
+        const uint32_t k2 = float_to_key(x.z), k3 = float_to_key(x.w);
+        const uint32_t pm = ok ? uint32_t(k0 <= theta) | (uint32_t(k1 <= theta) << 1) |
+                                     (uint32_t(k2 <= theta) << 2) | (uint32_t(k3 <= theta) << 3)
+                               : 0u;
+        if (__any_sync(kFullMask, pm != 0u)) {
+          // this lane's passing keys go to consecutive slots after those of
+          // the lanes below it: an inclusive warp scan of the counts, one
+          // atomic for the warp's total
+          const uint32_t cnt = __popc(pm);
+          uint32_t inc = cnt;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if ((pm >> j) & 1u) {
-            if (pos < uint32_t(cap)) {
-              ck[pos] = kk[j];
-              ci[pos] = c + j;
+          for (int o = 1; o < 32; o *= 2) {
+            const uint32_t v = __shfl_up_sync(kFullMask, inc, o);
+            if (lane >= o) inc += v;
+          }
+          uint32_t bs = 0;
+          if (lane == 31) bs = atomicAdd(&count_s, inc);
+          uint32_t pos = __shfl_sync(kFullMask, bs, 31) + inc - cnt;
+          const uint32_t c = uint32_t(i4 * 4);
+          const uint32_t kk[4] = {k0, k1, k2, k3};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if ((pm >> j) & 1u) {
+              if (pos < uint32_t(cap)) {
+                ck[pos] = kk[j];
+                ci[pos] = c + j;
+              }
+              ++pos;
             }
-            ++pos;
           }
         }
       }
