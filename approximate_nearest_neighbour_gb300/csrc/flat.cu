@@ -186,7 +186,7 @@ int knn_by_tiles(const float* Q, int64_t nq, const float* X, int64_t n, int d, i
 
   FilterPlan fp;
   if (filter_plan(n, k, &fp)) {
-    const int64_t G = 128 * int64_t(fp.split_a);
+    const int64_t G0 = 128 * int64_t(fp.split_a);
     // candidate segments: nseg per row from the filter pass's CTA split, each
     // holding 4x its expected share of ~1.5 k n / ns survivors (at least 64)
     auto seg_cap = [&](int nseg) {
@@ -196,13 +196,29 @@ int knn_by_tiles(const float* Q, int64_t nq, const float* X, int64_t n, int d, i
     int64_t tq = std::min(nq, int64_t(65535) * 128);
     for (;;) {
       const int nseg = 2 * tc_filter_split(tq, n);
-      const int64_t row_bytes = G * 4 + 4 + int64_t(nseg) * (seg_cap(nseg) * 8 + 4);
+      const int64_t row_bytes = 4 * G0 * 4 + 4 + int64_t(nseg) * (seg_cap(nseg) * 8 + 4);
       if (tq <= 128 || tq * row_bytes <= kTileBytes) break;
       tq = std::max<int64_t>(128, (tq / 2) / 128 * 128);
     }
     const int split_b = tc_filter_split(tq, n);
     const int nseg = 2 * split_b;
     const int cap_s = seg_cap(nseg);
+    // the first pass's CTAs per query tile: raised from split_a (up to 4x and
+    // its column tiles) until the last wave on the SMs is at least 90 % full,
+    // which only adds groups (a tighter bound); large coarse stage: 158 CTAs
+    // took two waves on 152 SMs
+    int split_a = fp.split_a;
+    {
+      const int64_t qtiles = ceil_div(tq, 128), sms = num_sms();
+      for (int64_t sa = fp.split_a; sa <= std::min<int64_t>(4 * fp.split_a, fp.ns / 128); ++sa) {
+        const int64_t ctas = qtiles * sa;
+        if (10 * ctas >= 9 * ceil_div(ctas, sms) * sms) {
+          split_a = int(sa);
+          break;
+        }
+      }
+    }
+    const int64_t G = 128 * int64_t(split_a);
     float* gmin = nullptr;
     float* bound = nullptr;
     uint64_t* cand = nullptr;
@@ -214,7 +230,7 @@ int knn_by_tiles(const float* Q, int64_t nq, const float* X, int64_t n, int d, i
     for (int64_t q0 = 0; q0 < nq; q0 += tq) {
       const int64_t rows = std::min(tq, nq - q0);
       IVFPQ_TRY(l2_tc_group_min(qo.hi + q0 * dpad, qo.lo + q0 * dpad, rows, xo.hi, xo.lo,
-                                xo.norms, fp.ns, d, fp.split_a, gmin, err, s));
+                                xo.norms, fp.ns, d, split_a, gmin, err, s));
       // a bound of each row's k-th smallest group minimum (radix selection;
       // the k-entry queues of a full selection took 4.7 ms of a 10,000-query
       // flat k = 1024 call)
