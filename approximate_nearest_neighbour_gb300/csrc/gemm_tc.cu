@@ -639,9 +639,25 @@ int run_tc(const float* qhi, const float* qlo, int64_t nq, const float* xhi, con
 }
 
 int default_split(int64_t nq, int64_t n) {
-  const int64_t qtiles = ceil_div(nq, TM), ntiles = ceil_div(n, TN);
-  return int(std::max<int64_t>(
-      1, std::min<int64_t>(ntiles, ceil_div(8 * int64_t(num_sms()), qtiles))));
+  const int64_t qtiles = ceil_div(nq, TM), ntiles = ceil_div(n, TN), sms = num_sms();
+  const int64_t s0 = std::max<int64_t>(1, std::min<int64_t>(ntiles, ceil_div(8 * sms, qtiles)));
+  // long CTAs (at least 64 column tiles each): up to twice the CTAs where
+  // that fills the last wave better (flat 1e6 x 128 with 10,000 queries: 16
+  // per query tile left the ninth wave 30 % full); short ones keep s0, their
+  // start-up (query tile load, TMEM allocation) outweighs the tail (the
+  // large workload's coarse pass took 1.43 -> 1.56 ms with twice the CTAs)
+  if (ntiles / s0 < 64) return int(s0);
+  int64_t best = s0;
+  double best_fill = 0.0;
+  for (int64_t sv = s0; sv <= std::min(ntiles, 2 * s0); ++sv) {
+    const int64_t ctas = qtiles * sv;
+    const double fill = double(ctas) / double(ceil_div(ctas, sms) * sms);
+    if (fill > best_fill + 1e-9) {
+      best_fill = fill;
+      best = sv;
+    }
+  }
+  return int(best);
 }
 }  // namespace
 
