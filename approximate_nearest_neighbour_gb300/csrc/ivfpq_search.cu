@@ -86,8 +86,13 @@ int try_scan2_kw(const ScanParams& p, int64_t nq, cudaStream_t s, int* launched)
                                                                    cudaStream_t);            \
   extern template int launch_scan_lm<MW, DS, 6, 0, IVFPQ_LUT_FP16>(const LmParams&,          \
                                                                    cudaStream_t);            \
+  extern template int launch_scan_lm<MW, DS, 4, 0, IVFPQ_LUT_FP8>(const LmParams&,           \
+                                                                  cudaStream_t);             \
+  extern template int launch_scan_lm<MW, DS, 8, 0, IVFPQ_LUT_FP8>(const LmParams&,           \
+                                                                  cudaStream_t);             \
   IVFPQ_EXTERN_SCAN_LM_LT(MW, DS, IVFPQ_LUT_FP32)                                            \
-  IVFPQ_EXTERN_SCAN_LM_LT(MW, DS, IVFPQ_LUT_FP16)
+  IVFPQ_EXTERN_SCAN_LM_LT(MW, DS, IVFPQ_LUT_FP16)                                            \
+  IVFPQ_EXTERN_SCAN_LM_LT(MW, DS, IVFPQ_LUT_FP8)
 IVFPQ_EXTERN_SCAN_LM(8, 3)
 IVFPQ_EXTERN_SCAN_LM(8, 4)
 IVFPQ_EXTERN_SCAN_LM(4, 8)
@@ -666,7 +671,7 @@ bool use_list_major(const ivfpq_index* ix, int64_t nq, int nprobe) {
   p.d = ix->d;
   p.k = 1;
   p.lut_type = ix->lut_type;
-  if (ix->lut_type == IVFPQ_LUT_FP16) p.lut_type = IVFPQ_LUT_FP32;  // by list: fp32 or binary16
+  p.lut_type = IVFPQ_LUT_FP32;  // by list: fp32, binary16 or E4M3 tables, the same shapes
   if (!scan2_shape(p)) return false;
   if (ix->scan_mode == 1) return true;
   return double(nq) * nprobe >= 2.0 * ix->nlist;
@@ -840,7 +845,9 @@ int scan_stage_lm(const ivfpq_index* ix, const float* queries, int64_t nq, int n
   IVFPQ_TRY(ws.alloc(&bp.part_key, size_t(max_items) * plen));
   int launched = 0;
   const bool half = ix->lut_type == IVFPQ_LUT_FP16;
+  const bool e4m3 = ix->lut_type == IVFPQ_LUT_FP8;
   if (half) IVFPQ_TRY(launch_bound_pass<IVFPQ_LUT_FP16>(bp, tq, s, &launched));
+  else if (e4m3) IVFPQ_TRY(launch_bound_pass<IVFPQ_LUT_FP8>(bp, tq, s, &launched));
   else IVFPQ_TRY(launch_bound_pass<IVFPQ_LUT_FP32>(bp, tq, s, &launched));
   IVFPQ_REQUIRE(launched, "scan: no list-major kernel for m=%d d/m=%d", ix->m, ix->dsub);
   uint32_t* theta = nullptr;
@@ -855,8 +862,10 @@ int scan_stage_lm(const ivfpq_index* ix, const float* queries, int64_t nq, int n
   // the fastest measured (search ms, 10,000 queries, 2 / 3 sets: fp32 large
   // 13.02 / 12.29; binary16 billion 21.40 / 20.06, large 10.73 / 10.66, mid
   // 7.72 / 8.45)
-  const int sets = ix->lm_group ? ix->lm_group : (half && ix->m == 16) ? 2 : 3;
-  const int G = sets * (half ? 2 : 1);
+  // (E4M3: four queries per set, at most two sets)
+  const int sets = e4m3 ? std::min(ix->lm_group ? ix->lm_group : 2, 2)
+                        : ix->lm_group ? ix->lm_group : (half && ix->m == 16) ? 2 : 3;
+  const int G = sets * (e4m3 ? 4 : half ? 2 : 1);
   IVFPQ_TRY(plan_items(probes, nq, nprobe, 0, nprobe, G, ix->nlist, ws, s, lp));
   const int cap = std::max(1024, 2 * k);
   lp.theta_key = theta;
@@ -904,7 +913,10 @@ int scan_stage_lm(const ivfpq_index* ix, const float* queries, int64_t nq, int n
   // stage timing: the bound pass and the planning count as stage 1, the
   // filter kernel alone as stage 2
   record(ix, 2, s);
-  if (half) {
+  if (e4m3) {
+    if (G >= 8) IVFPQ_TRY((try_scan_lm<8, 0, IVFPQ_LUT_FP8>(lp, s, &launched)));
+    else IVFPQ_TRY((try_scan_lm<4, 0, IVFPQ_LUT_FP8>(lp, s, &launched)));
+  } else if (half) {
     if (G >= 6) IVFPQ_TRY((try_scan_lm<6, 0, IVFPQ_LUT_FP16>(lp, s, &launched)));
     else IVFPQ_TRY((try_scan_lm<4, 0, IVFPQ_LUT_FP16>(lp, s, &launched)));
   } else {
@@ -1103,8 +1115,8 @@ extern "C" int ivfpq_set_scan_mode(ivfpq_index* ix, int mode, int group) {
   clear_error();
   IVFPQ_REQUIRE(ix, "ivfpq_set_scan_mode: null index");
   IVFPQ_REQUIRE(mode >= -1 && mode <= 1, "ivfpq_set_scan_mode: mode=%d outside [-1, 1]", mode);
-  IVFPQ_REQUIRE(group >= -1 && group <= 3 && group != 1,
-                "ivfpq_set_scan_mode: group=%d (0 keeps the current, -1 automatic, else 2 or 3)",
+  IVFPQ_REQUIRE(group >= -1 && group <= 3,
+                "ivfpq_set_scan_mode: group=%d (0 keeps the current, -1 automatic, else 1 to 3)",
                 group);
   ix->scan_mode = mode;
   if (group) ix->lm_group = group < 0 ? 0 : group;

@@ -89,6 +89,7 @@ struct LmHead {
   int64_t boff;
   int q[kLmMaxG];
   uint32_t theta[kLmMaxG];
+  float scale[kLmMaxG];  // E4M3 tables: each query's table scale (set by the build)
 };
 constexpr int kLmHead = 128;
 static_assert(sizeof(LmHead) <= kLmHead, "record head");
@@ -161,6 +162,36 @@ __device__ __forceinline__ void lm_lookups_h(const uint32_t (&w)[MW], const char
   }
 }
 
+// E4M3 tables: word (row, column) of table set g holds the entries of queries
+// 4g .. 4g + 3 (byte i: query 4g + i), each decoded exactly to binary16 and
+// added to its query's fp32 sum (mixed-precision add, one rounding).
+__device__ __forceinline__ void lm_add_h2(float& a, float& b, uint32_t h2) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+      : "+f"(a), "+f"(b)
+      : "r"(h2));
+}
+template <int MW, int NS, int NC, int P, int S = 0>
+__device__ __forceinline__ void lm_lookups_q8(const uint32_t (&w)[MW], const char* tab,
+                                              const uint32_t (&lcol)[MW], float (&acc)[4 * NS][4]) {
+  if constexpr (S < 4 * MW) {
+    constexpr int SEL = 0xCC00 | ((S & 3) << 4) | (4 + (S & 3));
+    const uint32_t off = lm_prmt<SEL>(w[S >> 2], lcol[S >> 2]);
+#pragma unroll
+    for (int g = 0; g < NS; ++g) {
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(tab + off + g * 65536 + 128 * P);
+      const __half2_raw h01 =
+          __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(v & 0xffffu), __NV_E4M3);
+      const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(__nv_fp8x2_storage_t(v >> 16), __NV_E4M3);
+      lm_add_h2(acc[4 * g][S % NC], acc[4 * g + 1][S % NC],
+                uint32_t(h01.x) | (uint32_t(h01.y) << 16));
+      lm_add_h2(acc[4 * g + 2][S % NC], acc[4 * g + 3][S % NC],
+                uint32_t(h23.x) | (uint32_t(h23.y) << 16));
+    }
+    lm_lookups_q8<MW, NS, NC, P, S + 1>(w, tab, lcol, acc);
+  }
+}
+
 // Per-query partial sums of one code block (acc[q][s & 3] over positions s).
 template <int NA>
 struct LmAcc {
@@ -200,10 +231,13 @@ __host__ __device__ constexpr int lm_prefetch_depth(int MW, int TQ) {
 template <int MW, int DS, int G, int TQ, int LT>
 __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const LmParams p) {
   static_assert(TQ == 0 || G == 1, "the bound pass takes one query per item");
-  static_assert(LT == IVFPQ_LUT_FP32 || LT == IVFPQ_LUT_FP16, "fp32 or binary16 tables");
+  static_assert(LT == IVFPQ_LUT_FP32 || LT == IVFPQ_LUT_FP16 || LT == IVFPQ_LUT_FP8,
+                "fp32, binary16 or E4M3 tables");
   static_assert(G <= kLmMaxG, "record head");
   constexpr bool H = LT == IVFPQ_LUT_FP16;
-  constexpr int NS = H ? (G + 1) / 2 : G;  // table sets
+  constexpr bool Q8 = LT == IVFPQ_LUT_FP8;
+  constexpr int QPS = Q8 ? 4 : H ? 2 : 1;     // queries per table set (entries per word)
+  constexpr int NS = (G + QPS - 1) / QPS;      // table sets
   using Sh = Scan2Shape<MW, DS>;
   constexpr int NW = kLmWarps;
   constexpr int m = Sh::M;
@@ -295,6 +329,70 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
     const LmHead& d = head(slot);
     const int nq = d.nq;
     const float* rs = resid(slot);
+    if constexpr (Q8) {
+      // E4M3: one scale per query's table, s = max T / 448 (the largest
+      // finite E4M3 value), entries E4M3(T * 448 / max T) (round to nearest
+      // even, saturating). The block-wide maximum first: each warp's maximum
+      // of its entries, then the entries again, quantized.
+      float* wmax = reinterpret_cast<float*>(slots + kLmSlots * p.rec_bytes);  // [NW][kLmMaxG]
+#pragma unroll
+      for (int q = 0; q < G; ++q) {
+        if (q >= nq) break;
+        float r[DS];
+#pragma unroll
+        for (int t = 0; t < DS; ++t) r[t] = rs[q * p.dpad + jj * DS + t];
+        float mx = 0.f;
+#pragma unroll
+        for (int s = 0; s < STEPS; ++s) mx = fmaxf(mx, entry(r, s));
+#pragma unroll
+        for (int o = 16; o >= 1; o /= 2) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, o));
+        if (lane == 0) wmax[warp * kLmMaxG + q] = mx;
+      }
+      __syncthreads();
+      LmHead* hw = reinterpret_cast<LmHead*>(slots + slot * p.rec_bytes);
+#pragma unroll
+      for (int g = 0; g < NS; ++g) {
+        if (4 * g >= nq) break;
+        uint32_t word[STEPS];
+#pragma unroll
+        for (int s = 0; s < STEPS; ++s) word[s] = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int q = 4 * g + i;
+          if (q < nq) {
+            float tmax = 0.f;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) tmax = fmaxf(tmax, wmax[w * kLmMaxG + q]);
+            const float inv = tmax > 0.f ? 448.f / tmax : 1.f;
+            if (tid == 0) hw->scale[q] = tmax > 0.f ? tmax / 448.f : 1.f;
+            float r[DS];
+#pragma unroll
+            for (int t = 0; t < DS; ++t) r[t] = rs[q * p.dpad + jj * DS + t];
+#pragma unroll
+            for (int s = 0; s < STEPS; ++s)
+              word[s] |= uint32_t(__nv_cvt_float_to_fp8(entry(r, s) * inv, __NV_SATFINITE,
+                                                        __NV_E4M3))
+                         << (8 * i);
+          } else {
+            // a missing query of the set: entries 448 and, in the scan, bound 0
+            if (tid == 0 && q < kLmMaxG) hw->scale[q] = 1.f;
+#pragma unroll
+            for (int s = 0; s < STEPS; ++s) word[s] |= 0x7Eu << (8 * i);
+          }
+        }
+        uint32_t* tg = reinterpret_cast<uint32_t*>(tab) + g * kGroupWords + 32 * P + jj;
+#pragma unroll
+        for (int s = 0; s < STEPS; ++s) {
+          const int e = (s * NW + warp) * QQ + qq;
+          uint32_t* row = tg + e * 64;
+          if (dcheck(sp.dbg, e >= 0 && e < 256, 7)) {
+#pragma unroll
+            for (int rep = 0; rep < REPS; ++rep) row[GS * ((rep + qq) & (REPS - 1))] = word[s];
+          }
+        }
+      }
+      return;
+    }
 #pragma unroll
     for (int g = 0; g < NS; ++g) {
       if ((H ? 2 * g : g) >= nq) break;
@@ -372,14 +470,17 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
     const int nqi = d.nq;
     int qv[GG];
     uint32_t th[GG];
+    float sc[GG];
 #pragma unroll
     for (int g = 0; g < GG; ++g) {
       // fp32 items are scanned with exactly their query count (GG = nqi);
-      // binary16 ones in whole pairs, so the last pair may have one query:
-      // the missing one has +inf table entries and bound 0, so nothing passes
-      const bool live = !H || g < nqi;
+      // binary16 / E4M3 ones in whole sets of 2 / 4, so the last set may be
+      // short: a missing query has +inf / 448 table entries and bound 0, so
+      // nothing passes
+      const bool live = QPS == 1 || g < nqi;
       qv[g] = live ? d.q[g] : d.q[0];
       th[g] = live ? d.theta[g] : 0u;
+      sc[g] = Q8 ? d.scale[g] : 1.f;
     }
     const bool in_range =
         dcheck(sp.dbg, boff >= 0 && boff + ((len + 31) >> 5) <= sp.nblocks, 4);
@@ -387,10 +488,11 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
     const uint8_t* lcodes = sp.codes + boff * 32 * m;
     // partial sums of a code block from its code words w
     auto score = [&](const uint32_t (&w)[MW]) {
-      LmAcc<H ? 2 * ((GG + 1) / 2) : GG> acc;
+      LmAcc<QPS * ((GG + QPS - 1) / QPS)> acc;
 #pragma unroll
       for (auto& a : acc.v) a[0] = a[1] = a[2] = a[3] = 0.f;
-      if constexpr (H) lm_lookups_h<MW, (GG + 1) / 2, (GG > 4 ? 2 : 4), P>(w, tab_bytes, lcol, acc.v);
+      if constexpr (Q8) lm_lookups_q8<MW, (GG + 3) / 4, (GG > 4 ? 2 : 4), P>(w, tab_bytes, lcol, acc.v);
+      else if constexpr (H) lm_lookups_h<MW, (GG + 1) / 2, (GG > 4 ? 2 : 4), P>(w, tab_bytes, lcol, acc.v);
       else lm_lookups<MW, GG, P>(w, tab_bytes, lcol, acc.v);
       return acc;
     };
@@ -399,7 +501,8 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
       const uint32_t slot_id = uint32_t((boff + b) * 32 + lane);
 #pragma unroll
       for (int g = 0; g < GG; ++g) {
-        const float dist = (acc.v[g][0] + acc.v[g][1]) + (acc.v[g][2] + acc.v[g][3]);
+        float dist = (acc.v[g][0] + acc.v[g][1]) + (acc.v[g][2] + acc.v[g][3]);
+        if constexpr (Q8) dist *= sc[g];
         if constexpr (TQ > 0) {
           const uint32_t key = valid ? __float_as_uint(dist) : kSentinelKey;
           if (key < tq[TQ - 1]) {
@@ -468,6 +571,14 @@ __global__ void __launch_bounds__(kLmWarps * 32, 1) ivfpq_scan_lm_kernel(const L
     const int nqc = head(cur).nq;
     if (TQ > 0 || nqc >= G) {
       scan(cur, Pc, std::integral_constant<int, G>{});
+    } else if constexpr (Q8) {
+      // E4M3: whole table sets (quadruples of queries)
+      if constexpr (G > 4) {
+        if (nqc > 4) scan(cur, Pc, std::integral_constant<int, 8>{});
+        else scan(cur, Pc, std::integral_constant<int, 4>{});
+      } else {
+        scan(cur, Pc, std::integral_constant<int, 4>{});
+      }
     } else if constexpr (H) {
       // binary16: whole table sets (pairs of queries)
       if constexpr (G > 4) {
@@ -509,8 +620,11 @@ inline size_t scan_lm_smem_bytes(int sets, int rec_bytes) {
 template <int MW, int DS, int G, int TQ, int LT>
 int launch_scan_lm(const LmParams& p, cudaStream_t s) {
   auto kern = ivfpq_scan_lm_kernel<MW, DS, G, TQ, LT>;
-  const int sets = LT == IVFPQ_LUT_FP16 ? (G + 1) / 2 : G;
-  const size_t smem = scan_lm_smem_bytes(sets, p.rec_bytes);
+  const int qps = LT == IVFPQ_LUT_FP8 ? 4 : LT == IVFPQ_LUT_FP16 ? 2 : 1;
+  const int sets = (G + qps - 1) / qps;
+  // E4M3 tables: the warps' table maxima follow the item records
+  const size_t smem = scan_lm_smem_bytes(sets, p.rec_bytes) +
+                      (LT == IVFPQ_LUT_FP8 ? size_t(kLmWarps) * kLmMaxG * 4 : 0);
   IVFPQ_TRY(set_dynamic_smem(kern, smem));
   kern<<<unsigned(num_sms()), kLmWarps * 32, smem, s>>>(p);
   IVFPQ_LAUNCHED_K(kern, smem, kLmWarps * 32);

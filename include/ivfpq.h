@@ -199,8 +199,8 @@ int ivfpq_set_precomputed(ivfpq_index* index, int mode);
  * scan; results are the same either way (up to the order of equal distances).
  * Source: "Billion-scale similarity search with GPUs", section 5: queries x
  * lists are independent work, taken there query by query.
- *  mode   -1 automatic (default): by list where the shapes allow it (fp32
- *            or binary16 tables, direct tables, (m, d/m) in {(32,3), (32,4),
+ *  mode   -1 automatic (default): by list where the shapes allow it (fp32,
+ *            binary16 or E4M3 tables, direct tables, (m, d/m) in {(32,3), (32,4),
  *            (16,8), (16,4), (8,12), (8,8)}, nprobe >= 2) and the batch
  *            probes every list twice or more on average, else by query;
  *          0 by query: one thread block per (query, chunk of its lists);
@@ -209,9 +209,11 @@ int ivfpq_set_precomputed(ivfpq_index* index, int mode);
  *            per item, each query keeping the codes within a bound taken
  *            from its nearest list (scanned first); a query with more such
  *            codes than its buffer holds is scanned again by query
- *  group  table sets per by-list item: 2 or 3 (a set holds one query's fp32
- *         tables or two queries' binary16 tables), -1 automatic (default:
- *         3, or 2 for binary16 tables with m = 16), 0 keeps the current value
+ *  group  table sets per by-list item: 1 to 3 (a set holds one query's fp32
+ *         tables, two queries' binary16 tables or four queries' E4M3 tables;
+ *         E4M3 items take at most 2 sets), -1 automatic (default: 3, or 2 for
+ *         binary16 tables with m = 16 and for E4M3 tables), 0 keeps the
+ *         current value
  * Errors: INVALID_ARG.
  */
 int ivfpq_set_scan_mode(ivfpq_index* index, int mode, int group);

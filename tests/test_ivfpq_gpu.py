@@ -171,6 +171,37 @@ def test_list_major_binary16_tables_follow_the_oracle_variant(B, m, dsub, group)
         assert np.all(np.abs(gd - qd) <= 1e-5 * np.abs(qd) + 1e-6), f"k={k}"
 
 
+@pytest.mark.parametrize("group", [1, 2])
+@pytest.mark.parametrize("m,dsub", LM_SHAPES)
+def test_list_major_e4m3_tables_follow_the_oracle_variant(B, m, dsub, group):
+    """The by-list scan with E4M3 tables (four queries' entries per
+    shared-memory word, one scale per query's table, fp32 sums of the decoded
+    entries) against the oracle's E4M3 tables: distances within the format's
+    precision, ids up to the near-ties its 3-bit mantissas make (the GPU
+    scales by 448 / max T where the oracle divides by max T / 448, so an entry
+    next to a rounding boundary may land one step apart; with k = 1 over 60
+    rows one swapped near-tie is 1.7 % of the recall)."""
+    import torch
+    w = S.IVFPQWorkload("t", 280 + m + dsub, 40_000, m * dsub, 61, m, 0.15, True, 300, (9,),
+                        (33,), ("fp8",))
+    data = S.compressed_index(w)
+    q = S.queries(w.number, data.cent, data.weights, w.sigma, w.nq)
+    ix = make_index(B, data.cent, data.cb, data.codes, data.list_ids, data.ids)
+    B.ivfpq_set_lut_type(ix, "fp8")
+    rows = np.arange(0, 300, 5)
+    for k in (1, 100, 700):
+        B.ivfpq_set_scan_mode(ix, 1, group)
+        gp, _ = B.ivfpq_search_probes(ix, _t(q), 9)
+        gd, gi = B.ivfpq_search(ix, _t(q), 9, k)
+        assert B.last_scan_kernel(ix) == "ivfpq_scan_lm_kernel"
+        torch.cuda.synchronize()
+        gp, gd, gi = (t.cpu().numpy() for t in (gp, gd, gi))
+        od, oi, _ = oracle.ivfpq_search(q[rows], data.cent, data.cb, data.list_off, data.codes,
+                                        data.ids, 9, k, oracle.LUT_FP8, forced_probes=gp[rows])
+        assert np.all(np.abs(gd[rows] - od) <= 3e-2 * np.abs(od) + 1e-5), f"k={k}"
+        assert oracle.recall_at_k(gi[rows], oi) >= (0.9 if k == 1 else 0.95), f"k={k}"
+
+
 @pytest.mark.parametrize("lut", ["fp32", "fp16"])
 def test_list_major_long_nearest_list_is_chunked(B, lut):
     """A nearest list longer than a bound-pass chunk (32,768 codes): its
