@@ -417,11 +417,12 @@ def run_ours(args):
         achieved = scan_bytes / (scan_ms / 1e3) / 1e9
         traffic = profiled_traffic(scan_kernel)
         # the look-up bound: one 4-byte shared-memory word per code byte and
-        # query, or per two queries where the by-list scan packs two binary16
-        # entries into a word
+        # query, or per two / four queries where the by-list scan packs two
+        # binary16 / four E4M3 entries into a word
         nsm = torch.cuda.get_device_properties(dev).multi_processor_count
         sm_mhz = sm_max_mhz()
-        per_word = 2 if (args.lut == "fp16" and scan_kernel == "ivfpq_scan_lm_kernel") else 1
+        per_word = ({"fp16": 2, "fp8": 4}.get(args.lut, 1)
+                    if scan_kernel == "ivfpq_scan_lm_kernel" else 1)
         lookup_peak = nsm * LOOKUPS_PER_SM_CLOCK * per_word * sm_mhz * 1e6
         lookups_per_s = scan_bytes / (scan_ms / 1e3)
         if traffic is not None and (args.n is not None or args.nlist is not None
