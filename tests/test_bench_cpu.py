@@ -53,3 +53,14 @@ def test_reference_arm_other_ranks_print_nothing(workload):
                   "--n", "4096", "--nq", "16", "--nlist", "64"],
                  {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert lines == []
+
+
+def test_reference_arm_takes_the_nprobe_override():
+    """--nprobe reaches the timed configuration: the metric and the config
+    name it (the mid workload states nprobe 16 and 64)."""
+    lines = _run(["--impl", "reference", "--workload", "mid", "--nprobe", "16", "--steps", "3",
+                  "--warmup", "3", "--n", "20000", "--nlist", "64", "--nq", "16"])
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert "nprobe=16" in d["metric"]
+    assert d["config"]["nprobe"] == 16
