@@ -3,12 +3,15 @@
 // and then, within that bin, by a histogram of the next 12 bits; the end of
 // that 256-key sub-bin is a bound theta with at least k keys <= theta and, on
 // spread-out keys, few more. The k smallest are then gathered (keys <= theta)
-// into shared memory and sorted with a bitonic network. Three uses where
-// WarpSelect's long queues (k > 256) cost most of the time:
+// into shared memory and sorted with a bitonic network (the helpers are in
+// select_radix.cuh). Uses here, where WarpSelect's queues cost most of the
+// time:
 //  * row_kth_bound: theta alone, an upper bound of each row's k-th smallest
-//    value (the filtered tensor-core plan's bound);
-//  * candidate selection over the filtered pass's segments for k > 256;
+//    value (the filtered tensor-core plan's bound, every k);
+//  * candidate selection over the filtered pass's segments for k > 32;
 //  * the final sort of the k re-ranked pairs of each row for k > 256.
+// (The by-list scan's final selection for k > 256 uses the same helpers, in
+// ivfpq_search.cu.)
 // A row whose gathered keys do not fit (ties around theta) or whose segment
 // overflowed is flagged; the caller redoes it with the full-length kernels.
 //
