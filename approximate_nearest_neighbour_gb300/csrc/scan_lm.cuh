@@ -13,9 +13,11 @@
 //  * one persistent block of 16 warps per SM takes items blockIdx.x,
 //    blockIdx.x + gridDim.x, ...; the 256 x m codewords stay in registers
 //    for the whole kernel (d/2 floats per thread, as in scan2.cuh);
-//  * shared memory holds G table sets, each a 256 x 64-word array whose two
-//    32-column halves are the double buffer: item t is scanned from half
-//    t & 1 while item t + 1's tables are built into the other half; a
+//  * shared memory holds the item's table sets (one query's fp32 tables,
+//    two queries' binary16 or four queries' E4M3 entries per 32-bit word),
+//    each a 256 x 64-word array whose two 32-column halves are the double
+//    buffer: item t is scanned from half t & 1 while item t + 1's tables are
+//    built into the other half; a
 //    column c of a half holds table c mod m, lane i reads column
 //    (i & ~(m-1)) | ((i + s) & (m-1)) at stored position s (table
 //    (i + s) mod m, the sub-quantizer of that stored byte), so the 32 lanes
@@ -25,6 +27,8 @@
 //    candidate buffer (one atomic per warp and query); the k smallest
 //    candidates are the query's result, and a query whose buffer overflows
 //    is scanned again by the general kernel;
+//  * a long list's records may be cut into units of unit_len codes (up to 16
+//    per record), so one list's items do not keep a few blocks busy alone;
 //  * the bound comes from a first pass of the same kernel over every query's
 //    nearest list alone (TQ > 0; one item per query and chunk of that list,
 //    the chunks at least 32,768 codes long and at most 4 per list, so a long
